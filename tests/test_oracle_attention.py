@@ -1,0 +1,60 @@
+"""Pins of the oracle's softmax attention against closed forms and invariants."""
+
+import numpy as np
+
+from oracle import attention as A
+
+
+def test_single_key_returns_its_value():
+    rng = np.random.default_rng(0)
+    q, k, v = rng.normal(size=4), rng.normal(size=(1, 4)), rng.normal(size=(1, 4))
+    assert np.array_equal(A.attend(q, k, v), v[0])
+
+
+def test_zero_query_is_the_mean_of_values():
+    rng = np.random.default_rng(1)
+    K, V = rng.normal(size=(7, 8)), rng.normal(size=(7, 8))
+    np.testing.assert_allclose(A.attend(np.zeros(8), K, V), V.mean(axis=0), rtol=0, atol=1e-15)
+
+
+def test_two_keys_closed_form_scale_is_inverse_sqrt_d():
+    # d = 4 so the scale is 1/2; logits 0 and ln 3 -> weights 1/4 and 3/4.
+    q = np.array([2 * np.log(3.0), 0, 0, 0])
+    K = np.array([[0.0, 5, -1, 2], [1.0, 5, -1, 2]]) * np.array([1, 0, 0, 0])
+    V = np.array([[4.0, 0, 0, 0], [0.0, 8, 0, 0]])
+    np.testing.assert_allclose(A.attention_weights(q, K), [0.25, 0.75], rtol=1e-15)
+    np.testing.assert_allclose(A.attend(q, K, V), [1.0, 6.0, 0, 0], rtol=1e-15, atol=1e-15)
+
+
+def test_permuting_cached_entries_does_not_change_output():
+    rng = np.random.default_rng(2)
+    q, K, V = rng.normal(size=16), rng.normal(size=(33, 16)), rng.normal(size=(33, 16))
+    perm = rng.permutation(33)
+    np.testing.assert_allclose(A.attend(q, K[perm], V[perm]), A.attend(q, K, V), rtol=1e-13)
+
+
+def test_logit_shift_invariance_and_large_logits():
+    # Adding the same logit to every key changes nothing, even when the logits are far
+    # beyond exp's range (the max-subtraction keeps it finite).
+    rng = np.random.default_rng(3)
+    q = rng.normal(size=8)
+    K, V = rng.normal(size=(9, 8)), rng.normal(size=(9, 8))
+    shift = 1000.0 * q / (q @ q) * np.sqrt(8)  # q . shift / sqrt(8) = 1000 for every key
+    np.testing.assert_allclose(A.attend(q, K + shift, V), A.attend(q, K, V), rtol=1e-10)
+
+
+def test_masked_route_equals_subset_route():
+    rng = np.random.default_rng(4)
+    q, K, V = rng.normal(size=8), rng.normal(size=(20, 8)), rng.normal(size=(20, 8))
+    vis = rng.random(20) < 0.4
+    vis[3] = True
+    np.testing.assert_allclose(A.attend_masked(q, K, V, vis), A.attend(q, K[vis], V[vis]),
+                               rtol=1e-13)
+
+
+def test_group_attention_is_per_head():
+    rng = np.random.default_rng(5)
+    qs, K, V = rng.normal(size=(4, 8)), rng.normal(size=(10, 8)), rng.normal(size=(10, 8))
+    out = A.attend_group(qs, K, V)
+    for g in range(4):
+        np.testing.assert_allclose(out[g], A.attend(qs[g], K, V), rtol=1e-15)

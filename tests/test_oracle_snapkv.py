@@ -1,0 +1,143 @@
+"""Pins of the SnapKV oracle: votes, pooling, top-k and selection.
+
+Each pin is something other than the oracle's own code: hand-worked examples
+(tests/golden), closed forms (harmonic sums for uniform attention), invariants
+(every softmax row sums to 1) and brute force over all subsets on tiny inputs.
+"""
+
+import itertools
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from conftest import fracs, read_golden
+from oracle import attention as A
+from oracle import snapkv as S
+
+
+def test_votes_hand_worked_example():
+    g = read_golden("votes_hand.txt")[0]
+    d, L, W = int(g["d"][0]), int(g["prompt_len"][0]), int(g["window"][0])
+    qs = [[float(x) for x in row[1:]] for row in g["_all"]["q"]]
+    assert [int(row[0]) for row in g["_all"]["q"]] == list(range(W))
+    q = np.array(qs)[None]
+    K = np.zeros((L, d))
+    K[:, 0] = np.log([float(x) for x in g["key_logs"]])
+    want = fracs(g["votes_num"], g["votes_den"])
+    got = S.window_votes(q, K)
+    np.testing.assert_allclose(got, [float(x) for x in want], rtol=1e-14)
+
+
+@pytest.mark.parametrize("G,Wq,L", [(1, 4, 9), (3, 5, 12), (2, 12, 12)])
+def test_votes_zero_query_harmonic_closed_form(G, Wq, L):
+    # q = 0: row at position p spreads 1/(p+1) over keys 0..p.
+    votes = S.window_votes(np.zeros((G, Wq, 6)), np.random.default_rng(0).normal(size=(L, 6)))
+    want = [sum(Fraction(G, p + 1) for p in range(L - Wq, L) if p >= j) for j in range(L)]
+    np.testing.assert_allclose(votes, [float(x) for x in want], rtol=1e-14)
+
+
+def test_votes_sum_to_number_of_rows_and_are_additive_over_heads():
+    rng = np.random.default_rng(1)
+    q, K = rng.normal(size=(3, 7, 16)), rng.normal(size=(40, 16)) * 2
+    v = S.window_votes(q, K)
+    assert abs(v.sum() - 21) < 1e-12
+    parts = sum(S.window_votes(q[g:g + 1], K) for g in range(3))
+    np.testing.assert_allclose(v, parts, rtol=1e-13)
+    assert (v >= 0).all()
+
+
+def test_votes_window_causality():
+    # Keys inside the window are seen only by window rows at or after them: the last
+    # key gets its whole vote from the last window row.
+    rng = np.random.default_rng(2)
+    q, K = rng.normal(size=(1, 4, 8)), rng.normal(size=(10, 8))
+    v = S.window_votes(q, K)
+    p_last = A.attention_weights(q[0, 3], K)
+    assert abs(v[9] - p_last[9]) < 1e-15
+
+
+def _golden_pool_cases():
+    return read_golden("pool_topk_hand.txt")
+
+
+@pytest.mark.parametrize("case", _golden_pool_cases(), ids=lambda c: c["name"])
+def test_pool_and_topk_hand_examples(case):
+    v = np.array([float(x) for x in case["v"]])
+    u = S.max_pool_1d(v, int(case["kernel"][0]))
+    np.testing.assert_array_equal(u, [float(x) for x in case["u"]])
+    keep = S.top_k_lowest_index(u, int(case["k"][0]))
+    np.testing.assert_array_equal(keep, [int(x) for x in case["keep"]])
+
+
+def test_pool_kernel_one_is_identity_and_huge_kernel_is_global_max():
+    rng = np.random.default_rng(3)
+    v = rng.random(11)
+    np.testing.assert_array_equal(S.max_pool_1d(v, 1), v)
+    np.testing.assert_array_equal(S.max_pool_1d(v, 21), np.full(11, v.max()))
+    with pytest.raises(ValueError):
+        S.max_pool_1d(v, 4)
+
+
+def test_topk_brute_force_all_subsets_with_ties():
+    # For every small vector with heavy ties, the returned set is the unique k-subset
+    # whose every member precedes every non-member in the order (larger u first,
+    # then lower position).
+    rng = np.random.default_rng(4)
+    for trial in range(300):
+        n = int(rng.integers(1, 8))
+        u = rng.integers(0, 3, size=n).astype(float)
+        k = int(rng.integers(0, n + 1))
+
+        def before(a, b):
+            return u[a] > u[b] or (u[a] == u[b] and a < b)
+
+        valid = [set(c) for c in itertools.combinations(range(n), k)
+                 if all(before(a, b) for a in c for b in range(n) if b not in c)]
+        assert len(valid) == 1
+        got = S.top_k_lowest_index(u, k)
+        assert set(got.tolist()) == valid[0]
+        assert list(got) == sorted(got)
+
+
+def test_select_positions_window_budget_and_identity():
+    rng = np.random.default_rng(5)
+    votes = rng.random(100)
+    pos = S.select_positions(votes, 100, 8, 7, 30)
+    assert len(pos) == 30
+    assert list(pos[-8:]) == list(range(92, 100))
+    assert list(pos[:22]) == sorted(pos[:22]) and pos[21] < 92
+    assert list(S.select_positions(votes, 100, 8, 7, 100)) == list(range(100))
+    assert list(S.select_positions(votes, 100, 8, 7, 500)) == list(range(100))
+    assert list(S.select_positions(votes, 6, 8, 7, 3)) == list(range(6))
+    assert list(S.select_positions(votes, 100, 8, 7, 8)) == list(range(92, 100))
+    with pytest.raises(ValueError):
+        S.select_positions(votes, 100, 8, 7, 7)
+
+
+def test_budget_at_least_prompt_reproduces_full_attention_exactly():
+    rng = np.random.default_rng(6)
+    L, d = 48, 16
+    q_win = rng.normal(size=(2, 8, d))
+    K, V = rng.normal(size=(L, d)), rng.normal(size=(L, d))
+    pos, Kc, Vc, _ = S.compress_unit(q_win, K, V, 8, 7, L)
+    q = rng.normal(size=d)
+    assert np.array_equal(A.attend(q, Kc, Vc), A.attend(q, K, V))
+
+
+def test_group_mapping_query_head_to_kv_head():
+    # Hq = 4, Hkv = 2: query heads 2, 3 belong to KV head 1.  A query that aims at a
+    # planted key is placed only in head 3; that key must win the vote of KV head 1.
+    rng = np.random.default_rng(7)
+    B, Hq, Hkv, L, W, d = 1, 4, 2, 64, 4, 16
+    Q = rng.normal(size=(B, Hq, W, d)) * 0.1
+    K = rng.normal(size=(B, Hkv, L, d)) * 0.1
+    V = rng.normal(size=(B, Hkv, L, d))
+    aim = rng.normal(size=d)
+    Q[0, 3] += 4 * aim
+    K[0, 1, 17] += 4 * aim
+    res = S.compress(Q, K, V, W, 1, W + 1)
+    pos1, _, _, votes1 = res[0][1]
+    assert pos1[0] == 17 and votes1[:L - W].argmax() == 17
+    pos0, _, _, votes0 = res[0][0]
+    assert votes0[17] < 0.5 * votes1[17]
