@@ -1,0 +1,12 @@
+"""GB300 (sm_103a) attention-score KV-cache compression: SnapKV, H2O, StreamingLLM.
+
+The compute lives in libkvcompress.so (hand-written CUDA kernels behind the C ABI of
+include/kvcompress.h); this package is its thin Python binding.  See _binding for the
+entry points, which keep the C names.
+"""
+
+from ._binding import (  # noqa: F401
+    DEV_BAD_STATE, DEV_CACHE_FULL, DEV_TIMEOUT, H2OState, KVCError, compressed_decode_attn,
+    h2o_decode_step, h2o_prefill, kvc_device_status, kvc_selftest_wait_timeout,
+    kvc_set_wait_timeout_ns, kvc_version, lib, library_path, sink_window_append,
+    snapkv_compress, snapkv_workspace_bytes)

@@ -1,0 +1,329 @@
+// H2O decode step (H2O article, 処理の流れ: every decode step's attention over the
+// cache updates each cached token's cumulative score; over budget, heavy hitters and
+// the recent window are kept and the rest is evicted; 何を残すのか: heavy hitters +
+// recent tokens).
+//
+// One CTA per (layer, batch, KV head) unit, one pass over the cache:
+//   1. logits of the G query heads against every live row (the new token's row comes
+//      straight from k_new, so nothing waits on its write);
+//   2. exact softmax normaliser per head (block reduction);
+//   3. o = P.V with lanes over the head dim, merged over the 8 warps;
+//   4. score[e] += sum_g p_g[e] (the new entry starts from 0);
+//   5. if the unit now holds every slot: evict the smallest score among positions
+//      <= t - n_recent, the higher position on exact ties; its slot becomes free.
+// The step is HBM-bound: each live K and V row is read once (plus 12 bytes of score
+// and position per entry).
+#include <math.h>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int NT = 256;
+constexpr int NW = NT / 32;
+
+struct H2OP {
+  const __nv_bfloat16 *q, *k_new, *v_new;
+  __nv_bfloat16 *k, *v;
+  float *score;
+  int32_t *pos, *n_used, *free_slot;
+  __nv_bfloat16 *out;
+  int32_t *evicted;
+  int slots, n_recent, t;
+  float c;  // log2(e)/sqrt(D)
+  uint32_t *status;
+};
+
+template <int D>
+__device__ __forceinline__ void load_row(const __nv_bfloat16 *row, int lane, float (&f)[D / 32]) {
+  if (D == 128) {
+    const uint2 w = *reinterpret_cast<const uint2 *>(row + 4 * lane);
+    f[0] = bf_lo(w.x);
+    f[1] = bf_hi(w.x);
+    f[2 % (D / 32)] = bf_lo(w.y);
+    f[3 % (D / 32)] = bf_hi(w.y);
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(row + 2 * lane);
+    f[0] = bf_lo(w);
+    f[1 % (D / 32)] = bf_hi(w);
+  }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(NT) h2o_step_kernel(const H2OP p) {
+  constexpr int DV = D / 32;
+  extern __shared__ float hs[];
+  float *qs = hs;                         // [G][D]
+  float *lg = qs + G * D;                 // [G][slots]: logits, then probabilities
+  float *red = lg + G * p.slots;          // [NW][G][D]
+  __shared__ float wred[NW][G];
+  __shared__ float gstat[2][G];           // max, sum
+  __shared__ float es[NW];
+  __shared__ int ep[NW], eslot[NW];
+
+  const int u = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = p.slots;
+  const int f = p.free_slot[u], nu = p.n_used[u];
+  if (f < 0 || f >= S || nu < 0 || nu >= S || (nu < S - 1 && f != nu)) {
+    if (tid == 0) set_status(p.status, KVC_DEV_BAD_STATE);
+    return;
+  }
+  const int count = nu + 1;  // live rows 0..count-1, the new token at slot f
+  const size_t rowbase = (size_t)u * S;
+
+  for (int e = tid; e < G * D; e += NT)
+    qs[e] = __bfloat162float(p.q[(size_t)u * G * D + e]) * p.c;
+  __syncthreads();
+
+  // 1. logits: warp per row, lanes over the head dim
+  float qreg[G][DV];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int d = 0; d < DV; ++d) qreg[g][d] = qs[g * D + lane * DV + d];
+  for (int e0 = warp; e0 < count; e0 += 4 * NW) {
+    float kf[4][DV];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = e0 + i * NW;
+      if (e < count) {
+        const __nv_bfloat16 *src = (e == f) ? p.k_new + (size_t)u * D : p.k + (rowbase + e) * D;
+        load_row<D>(src, lane, kf[i]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = e0 + i * NW;
+      if (e >= count) break;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float a = 0.f;
+#pragma unroll
+        for (int d = 0; d < DV; ++d) a = fmaf(qreg[g][d], kf[i][d], a);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane == 0) lg[g * S + e] = a;
+      }
+    }
+  }
+  __syncthreads();
+
+  // 2. per-head max and normaliser
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float mx = -INFINITY;
+    for (int e = tid; e < count; e += NT) mx = fmaxf(mx, lg[g * S + e]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) wred[warp][g] = mx;
+  }
+  __syncthreads();
+  if (tid < G) {
+    float mx = -INFINITY;
+    for (int w = 0; w < NW; ++w) mx = fmaxf(mx, wred[w][tid]);
+    gstat[0][tid] = mx;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float M = gstat[0][g];
+    float sm = 0.f;
+    for (int e = tid; e < count; e += NT) {
+      const float x = ex2(lg[g * S + e] - M);
+      lg[g * S + e] = x;
+      sm += x;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+    if (lane == 0) wred[warp][g] = sm;
+  }
+  __syncthreads();
+  if (tid < G) {
+    float sm = 0.f;
+    for (int w = 0; w < NW; ++w) sm += wred[w][tid];
+    gstat[1][tid] = 1.f / sm;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float inv = gstat[1][g];
+    for (int e = tid; e < count; e += NT) lg[g * S + e] *= inv;
+  }
+  __syncthreads();
+
+  // 3. o = P.V
+  float o[G][DV];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int d = 0; d < DV; ++d) o[g][d] = 0.f;
+  for (int e0 = warp; e0 < count; e0 += 4 * NW) {
+    float vf[4][DV];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = e0 + i * NW;
+      if (e < count) {
+        const __nv_bfloat16 *src = (e == f) ? p.v_new + (size_t)u * D : p.v + (rowbase + e) * D;
+        load_row<D>(src, lane, vf[i]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = e0 + i * NW;
+      if (e >= count) break;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float pe = lg[g * S + e];
+#pragma unroll
+        for (int d = 0; d < DV; ++d) o[g][d] = fmaf(pe, vf[i][d], o[g][d]);
+      }
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int d = 0; d < DV; ++d) red[(warp * G + g) * D + lane * DV + d] = o[g][d];
+
+  // 4. scores; 5. eviction candidates (per-thread best, then block reduction)
+  float best_s = INFINITY;
+  int best_p = -1, best_e = -1;
+  const int thresh = p.t - p.n_recent;
+  for (int e = tid; e < count; e += NT) {
+    float add = 0.f;
+#pragma unroll
+    for (int g = 0; g < G; ++g) add += lg[g * S + e];
+    const float sc = (e == f ? 0.f : p.score[rowbase + e]) + add;
+    p.score[rowbase + e] = sc;
+    const int ps = (e == f) ? p.t : p.pos[rowbase + e];
+    if (count == S && ps <= thresh) {
+      if (sc < best_s || (sc == best_s && ps > best_p)) {
+        best_s = sc;
+        best_p = ps;
+        best_e = e;
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < G * D; e += NT) {
+    const int g = e / D, d = e - g * D;
+    float a = 0.f;
+    for (int w = 0; w < NW; ++w) a += red[(w * G + g) * D + d];
+    p.out[(size_t)u * G * D + e] = __float2bfloat16(a);
+  }
+#pragma unroll
+  for (int o2 = 16; o2 > 0; o2 >>= 1) {
+    const float s2 = __shfl_xor_sync(0xffffffffu, best_s, o2);
+    const int p2 = __shfl_xor_sync(0xffffffffu, best_p, o2);
+    const int e2 = __shfl_xor_sync(0xffffffffu, best_e, o2);
+    if (e2 >= 0 && (best_e < 0 || s2 < best_s || (s2 == best_s && p2 > best_p))) {
+      best_s = s2;
+      best_p = p2;
+      best_e = e2;
+    }
+  }
+  if (lane == 0) {
+    es[warp] = best_s;
+    ep[warp] = best_p;
+    eslot[warp] = best_e;
+  }
+  // new token's row
+  for (int e = tid; e < D / 8; e += NT) {
+    reinterpret_cast<uint4 *>(p.k + (rowbase + f) * D)[e] =
+        reinterpret_cast<const uint4 *>(p.k_new + (size_t)u * D)[e];
+    reinterpret_cast<uint4 *>(p.v + (rowbase + f) * D)[e] =
+        reinterpret_cast<const uint4 *>(p.v_new + (size_t)u * D)[e];
+  }
+  __syncthreads();
+  if (tid == 0) {
+    p.pos[rowbase + f] = p.t;
+    int victim = -1, vpos = -1;
+    float vs = INFINITY;
+    for (int w = 0; w < NW; ++w) {
+      if (eslot[w] < 0) continue;
+      if (victim < 0 || es[w] < vs || (es[w] == vs && ep[w] > vpos)) {
+        victim = eslot[w];
+        vpos = ep[w];
+        vs = es[w];
+      }
+    }
+    if (count == S) {
+      if (victim < 0) {  // cannot happen with n_recent < S; keep the state consistent
+        set_status(p.status, KVC_DEV_BAD_STATE);
+        victim = f == 0 ? 1 % S : 0;
+        vpos = p.pos[rowbase + victim];
+      }
+      p.free_slot[u] = victim;
+      p.n_used[u] = S - 1;
+      if (p.evicted) p.evicted[u] = vpos;
+    } else {
+      p.free_slot[u] = count;
+      p.n_used[u] = count;
+      if (p.evicted) p.evicted[u] = -1;
+    }
+  }
+}
+
+__global__ void h2o_init_kernel(int32_t *n_used, int32_t *free_slot, const int32_t *n_valid,
+                                int units) {
+  const int u = blockIdx.x * blockDim.x + threadIdx.x;
+  if (u < units) {
+    n_used[u] = n_valid[u];
+    free_slot[u] = n_valid[u];
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_t(const Ctx &c, const H2OArgs &a, const H2OP &p) {
+  const size_t smem = ((size_t)G * D + (size_t)G * a.slots + (size_t)NW * G * D) * sizeof(float);
+  static bool attr[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (smem > 48 * 1024 && dev < 64 && !attr[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(h2o_step_kernel<D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    attr[dev] = true;
+  }
+  h2o_step_kernel<D, G><<<a.units, NT, smem, c.stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_h2o_step(const Ctx &c, const H2OArgs &a) {
+  H2OP p;
+  p.q = reinterpret_cast<const __nv_bfloat16 *>(a.q);
+  p.k_new = reinterpret_cast<const __nv_bfloat16 *>(a.k_new);
+  p.v_new = reinterpret_cast<const __nv_bfloat16 *>(a.v_new);
+  p.k = reinterpret_cast<__nv_bfloat16 *>(a.k);
+  p.v = reinterpret_cast<__nv_bfloat16 *>(a.v);
+  p.score = a.score;
+  p.pos = a.pos;
+  p.n_used = a.n_used;
+  p.free_slot = a.free_slot;
+  p.out = reinterpret_cast<__nv_bfloat16 *>(a.out);
+  p.evicted = a.evicted;
+  p.slots = a.slots;
+  p.n_recent = a.n_recent;
+  p.t = a.t;
+  p.c = (float)(1.4426950408889634 / sqrt((double)a.D));
+  p.status = c.status;
+#define KVC_H2O(DD, GG) \
+  if (a.D == DD && a.G == GG) return launch_t<DD, GG>(c, a, p);
+  KVC_H2O(128, 1) KVC_H2O(128, 2) KVC_H2O(128, 4) KVC_H2O(128, 8)
+  KVC_H2O(64, 1) KVC_H2O(64, 2) KVC_H2O(64, 4) KVC_H2O(64, 8)
+#undef KVC_H2O
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_h2o_init_state(const Ctx &c, int32_t *pos, int32_t *n_used,
+                                  int32_t *free_slot, const int32_t *n_valid, int units,
+                                  int slots) {
+  (void)pos;
+  (void)slots;
+  h2o_init_kernel<<<(units + 255) / 256, 256, 0, c.stream>>>(n_used, free_slot, n_valid, units);
+  return cudaGetLastError();
+}
+
+}  // namespace kvc

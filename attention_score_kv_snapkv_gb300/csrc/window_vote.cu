@@ -1,0 +1,584 @@
+// SnapKV steps 1-2 (SnapKV article, 処理の流れ steps 1 and 2): every trailing window
+// query of the G query heads of a KV head takes softmax(q . k / sqrt(D)) over the keys
+// it may see (all keys up to and including its own position), and the probabilities
+// are summed per key into the vote.  With every prompt query as a "window" query this
+// is also H2O's initial cumulative score (causal column sums of the prompt attention).
+//
+// Design (sm_103a):
+// * A job is (unit u, tile of up to 128 query rows).  Its key range is cut into
+//   128-key tiles; the tiles are split over a group of g CTAs of a persistent,
+//   cooperatively launched grid (one CTA per SM).
+// * Pass 1, per key tile: S = Q . K^T on the tensor cores (tcgen05.mma, M = 128 query
+//   rows, N = 128 keys, fp32 accumulator in TMEM).  Warpgroup 0 (one thread per row)
+//   keeps each row's running max m and normaliser z (log2 domain).
+// * Row statistics are combined across the g CTAs of the job through global memory
+//   (the last CTA to arrive combines and publishes; bounded spin for the others).
+// * Pass 2, per key tile: S^T = K . Q^T (M = 128 keys, N = rows rounded up to 16);
+//   warpgroup 1 (one thread per key) sums exp2(s*c - (m + log2 z)) over its rows in
+//   registers -- no cross-lane reduction -- and writes the vote.
+// * Pass 2 of job k is interleaved with pass 1 of job k+1 (after a lead of two
+//   tiles), so the re-read of job k's keys comes from L2 and the statistics exchange
+//   is hidden behind useful work.
+// * Warp roles: warp 0 = TMA producer (Q tiles double-buffered, K tiles in a 4-stage
+//   ring, 128-byte swizzle), warp 1 = TMEM owner and MMA issuer, warps 2-5 = pass 1,
+//   warps 6-9 = pass 2.  Every wait is bounded (KVC_DEV_TIMEOUT on expiry).
+#include <math.h>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int TILE = 128;       // keys per tile; query rows per job
+constexpr int NSTAGE = 4;       // K tile ring depth
+constexpr int NTHREADS = 320;   // 10 warps
+constexpr int TMEM_COLS = 512;  // 4 accumulators of 128 fp32 columns
+constexpr int LEAD = 2;         // pass-1 tiles of job k+1 issued before pass 2 of job k
+
+template <int D>
+struct Geo {
+  static constexpr int KB = D / 64;           // 128-byte k-blocks per row
+  static constexpr int KBLK = TILE * 128;     // bytes of one k-block of a 128-row tile
+  static constexpr int TILE_BYTES = KB * KBLK;
+  static constexpr int OFF_Q = 0;             // 2 Q tiles
+  static constexpr int OFF_K = 2 * TILE_BYTES;
+  static constexpr int OFF_CTRL = OFF_K + NSTAGE * TILE_BYTES;
+  static constexpr int CTRL_BYTES = 4096;
+  static constexpr int NEED = OFF_CTRL + CTRL_BYTES + 1024;  // + base alignment slack
+  // At least 116 KB so that two CTAs never share an SM: each CTA allocates all 512
+  // TMEM columns, and the persistent grid relies on one resident CTA per SM.
+  static constexpr int SMEM = NEED > 116 * 1024 ? NEED : 116 * 1024;
+};
+
+// control-region byte offsets
+constexpr int C_QFULL = 0;      // 2 barriers
+constexpr int C_QEMPTY = 16;    // 2
+constexpr int C_KFULL = 32;     // NSTAGE
+constexpr int C_KEMPTY = 64;    // NSTAGE
+constexpr int C_SFULL = 96;     // 4 (TMEM accumulators)
+constexpr int C_SEMPTY = 128;   // 4
+constexpr int C_XFULL = 160;    // 2 (local statistics hand-off, g == 1)
+constexpr int C_XEMPTY = 176;   // 2
+constexpr int C_TMEM = 192;
+constexpr int C_ABORT = 196;
+constexpr int C_LAST = 200;
+constexpr int C_XSTAT = 256;    // float2 [2][128]  (2048 B)
+constexpr int C_OFF = 2304;     // float [128]
+constexpr int C_ROWPOS = 2816;  // int [128]
+constexpr int C_GO = 3328;      // int: pass-2 warpgroup may proceed (g > 1)
+
+struct WVP {
+  int L, R, Wq, row_tiles, jobs, g, ngroups;
+  float c;               // log2(e) / sqrt(D)
+  float *votes;          // [units, L]
+  int atomic_votes;      // several row tiles add into the same votes
+  float2 *part;          // [jobs][g][128] per-CTA row statistics (g > 1)
+  float2 *fin;           // [jobs][128] combined statistics (g > 1)
+  int *arrive;           // [jobs] arrival counters (zeroed before launch)
+  int *ready;            // [jobs] published flags (zeroed before launch)
+  uint32_t *status;
+  unsigned long long timeout;
+};
+
+struct Job {
+  int u, rho0, nrows, rpad, t0, t1, pmin, kend;
+};
+
+__device__ __forceinline__ Job job_geo(const WVP &p, int j, int xg) {
+  Job J;
+  J.u = j / p.row_tiles;
+  const int rt = j - J.u * p.row_tiles;
+  J.rho0 = rt * TILE;
+  J.nrows = min(TILE, p.R - J.rho0);
+  J.rpad = (J.nrows + 15) & ~15;
+  const int r0 = J.rho0 % p.Wq;
+  const bool wraps = (r0 + J.nrows) > p.Wq;
+  const int rmax = wraps ? p.Wq - 1 : r0 + J.nrows - 1;
+  const int rmin = wraps ? 0 : r0;
+  J.kend = p.L - p.Wq + rmax + 1;
+  J.pmin = p.L - p.Wq + rmin;
+  const int nkt = (J.kend + TILE - 1) / TILE;
+  J.t0 = (int)(((long long)xg * nkt) / p.g);
+  J.t1 = (int)(((long long)(xg + 1) * nkt) / p.g);
+  return J;
+}
+
+// Order of the tile events of one round: first LEAD pass-1 tiles of the new job (A),
+// then alternate pass-2 tiles of the previous job (B) and pass-1 tiles.
+__device__ __forceinline__ bool next_is_a(int ia, int ib, int na, int nb) {
+  if (ia >= na) return false;
+  if (ib >= nb) return true;
+  return ia < LEAD || (ia - LEAD) < ib;
+}
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    window_vote_kernel(const __grid_constant__ CUtensorMap tq,
+                       const __grid_constant__ CUtensorMap tk, const WVP p) {
+  using G = Geo<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t sQ = sb + G::OFF_Q, sK = sb + G::OFF_K, ctl = sb + G::OFF_CTRL;
+  uint8_t *ctrl = smem + G::OFF_CTRL;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctrl + C_TMEM);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl + C_ABORT);
+  volatile int *last_flag = reinterpret_cast<volatile int *>(ctrl + C_LAST);
+  float2 *xstat = reinterpret_cast<float2 *>(ctrl + C_XSTAT);
+  float *off = reinterpret_cast<float *>(ctrl + C_OFF);
+  int *rowpos = reinterpret_cast<int *>(ctrl + C_ROWPOS);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Abort ab{abort_flag, p.status, p.timeout};
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(ctl + C_QFULL + 8 * i, 1);
+      mbar_init(ctl + C_QEMPTY + 8 * i, 1);
+      mbar_init(ctl + C_XFULL + 8 * i, 4);
+      mbar_init(ctl + C_XEMPTY + 8 * i, 4);
+    }
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(ctl + C_KFULL + 8 * s, 1);
+      mbar_init(ctl + C_KEMPTY + 8 * s, 1);
+    }
+    for (int b = 0; b < 4; ++b) {
+      mbar_init(ctl + C_SFULL + 8 * b, 1);
+      mbar_init(ctl + C_SEMPTY + 8 * b, 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int gamma = blockIdx.x / p.g, xg = blockIdx.x - gamma * p.g;
+  const int njobs = gamma < p.jobs ? (p.jobs - gamma + p.ngroups - 1) / p.ngroups : 0;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      int kit = 0, qcnt[2] = {0, 0};
+      bool ok = true;
+      Job Jb{};
+      for (int k = 0; k <= njobs && ok; ++k) {
+        Job Ja{};
+        int na = 0, nb = 0;
+        if (k < njobs) {
+          Ja = job_geo(p, gamma + k * p.ngroups, xg);
+          na = Ja.t1 - Ja.t0;
+        }
+        if (k >= 1) nb = Jb.t1 - Jb.t0;
+        if (na > 0) {  // Q tile of job k into buffer k & 1
+          const int qb = k & 1;
+          if (!ab.wait(ctl + C_QEMPTY + 8 * qb, (qcnt[qb] & 1) ^ 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(ctl + C_QFULL + 8 * qb, G::TILE_BYTES);
+          for (int kb = 0; kb < G::KB; ++kb)
+            tma_load_2d(sQ + qb * G::TILE_BYTES + kb * G::KBLK, &tq, kb * 64,
+                        Ja.u * p.R + Ja.rho0, ctl + C_QFULL + 8 * qb);
+          ++qcnt[qb];
+        }
+        for (int ia = 0, ib = 0; ia < na || ib < nb;) {
+          int row;
+          if (next_is_a(ia, ib, na, nb)) {
+            row = Ja.u * p.L + (Ja.t0 + ia) * TILE;
+            ++ia;
+          } else {
+            row = Jb.u * p.L + (Jb.t1 - 1 - ib) * TILE;
+            ++ib;
+          }
+          const int s = kit % NSTAGE, use = kit / NSTAGE;
+          if (!ab.wait(ctl + C_KEMPTY + 8 * s, (use & 1) ^ 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(ctl + C_KFULL + 8 * s, G::TILE_BYTES);
+          for (int kb = 0; kb < G::KB; ++kb)
+            tma_load_2d(sK + s * G::TILE_BYTES + kb * G::KBLK, &tk, kb * 64, row,
+                        ctl + C_KFULL + 8 * s);
+          ++kit;
+        }
+        Jb = Ja;
+      }
+      // drain: every issued copy must have landed before the CTA may exit
+      for (int s = 0; s < NSTAGE; ++s) {
+        const int cnt = kit / NSTAGE + (s < kit % NSTAGE ? 1 : 0);
+        if (cnt > 0) mbar_wait_bounded(ctl + C_KFULL + 8 * s, (cnt - 1) & 1, p.timeout);
+      }
+      for (int qb = 0; qb < 2; ++qb)
+        if (qcnt[qb] > 0) mbar_wait_bounded(ctl + C_QFULL + 8 * qb, (qcnt[qb] - 1) & 1, p.timeout);
+    }
+  } else if (warp == 1) {
+    // -------------------------------- MMA issuer -------------------------------
+    if (lane == 0) {
+      int kit = 0, it1 = 0, it2 = 0, last_bar = -1, last_par = 0, qcnt[2] = {0, 0};
+      bool ok = true;
+      const uint32_t idesc1 = idesc_bf16(128, TILE);
+      Job Jb{};
+      for (int k = 0; k <= njobs && ok; ++k) {
+        Job Ja{};
+        int na = 0, nb = 0;
+        if (k < njobs) {
+          Ja = job_geo(p, gamma + k * p.ngroups, xg);
+          na = Ja.t1 - Ja.t0;
+        }
+        if (k >= 1) nb = Jb.t1 - Jb.t0;
+        if (na > 0) {
+          if (!ab.wait(ctl + C_QFULL + 8 * (k & 1), qcnt[k & 1] & 1)) { ok = false; break; }
+          ++qcnt[k & 1];
+          tc_fence_after();
+        }
+        const uint32_t idesc2 = idesc_bf16(128, Jb.rpad > 0 ? Jb.rpad : 16);
+        for (int ia = 0, ib = 0; ia < na || ib < nb;) {
+          const bool isa = next_is_a(ia, ib, na, nb);
+          int b, use;
+          if (isa) { b = it1 & 1; use = it1 >> 1; }
+          else { b = 2 + (it2 & 1); use = it2 >> 1; }
+          const int s = kit % NSTAGE, kuse = kit / NSTAGE;
+          if (!ab.wait(ctl + C_KFULL + 8 * s, kuse & 1)) { ok = false; break; }
+          if (!ab.wait(ctl + C_SEMPTY + 8 * b, (use & 1) ^ 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d = tmem + (uint32_t)(b * 128);
+          const uint32_t qa = sQ + (isa ? (k & 1) : ((k - 1) & 1)) * G::TILE_BYTES;
+          const uint32_t ka = sK + s * G::TILE_BYTES;
+#pragma unroll
+          for (int kb = 0; kb < G::KB; ++kb) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t o = kb * G::KBLK + kk * 32;
+              if (isa)
+                umma_bf16(d, sdesc_k128(qa + o), sdesc_k128(ka + o), idesc1, (kb | kk) != 0);
+              else
+                umma_bf16(d, sdesc_k128(ka + o), sdesc_k128(qa + o), idesc2, (kb | kk) != 0);
+            }
+          }
+          umma_commit(ctl + C_KEMPTY + 8 * s);
+          umma_commit(ctl + C_SFULL + 8 * b);
+          last_bar = b;
+          last_par = use & 1;
+          ++kit;
+          if (isa) { ++ia; ++it1; } else { ++ib; ++it2; }
+        }
+        if (!ok) break;
+        if (nb > 0) umma_commit(ctl + C_QEMPTY + 8 * ((k - 1) & 1));  // job k-1 done with Q
+        Jb = Ja;
+      }
+      // drain: wait for the completion of the last MMA batch issued
+      if (last_bar >= 0) mbar_wait_bounded(ctl + C_SFULL + 8 * last_bar, last_par, p.timeout);
+    }
+  } else if (warp < 6) {
+    // ------------------ pass 1: row statistics (one thread per row) ------------------
+    // Control flow (loops, named barriers) is identical for every thread of the
+    // warpgroup; a failed wait only turns the remaining work off (ok = false).
+    const int quarter = warp & 3;
+    const int lrow = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    int it1 = 0;
+    bool ok = true;
+    for (int k = 0; k < njobs; ++k) {
+      const int j = gamma + k * p.ngroups;
+      const Job J = job_geo(p, j, xg);
+      const int n = J.t1 - J.t0;
+      const bool rvalid = lrow < J.nrows;
+      const int prow = rvalid ? p.L - p.Wq + (J.rho0 + lrow) % p.Wq : -1;
+      const bool warp_active = quarter * 32 < J.nrows;
+      float m = -INFINITY, z = 0.f;
+      for (int i = 0; i < n; ++i, ++it1) {
+        const int b = it1 & 1;
+        const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_SFULL + 8 * b, (it1 >> 1) & 1));
+        ok = got;
+        if (!got) continue;
+        tc_fence_after();
+        if (warp_active) {
+          const int kbase = (J.t0 + i) * TILE;
+          const bool full = kbase + TILE - 1 <= prow;
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            float s[64];
+            tmem_ld32(tmem + lane_base + (uint32_t)(b * 128 + h * 64), s);
+            tmem_ld32(tmem + lane_base + (uint32_t)(b * 128 + h * 64 + 32), s + 32);
+            tmem_wait_ld();
+            if (!full) {
+#pragma unroll
+              for (int c = 0; c < 64; ++c)
+                if (kbase + h * 64 + c > prow) s[c] = -INFINITY;
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < 64; ++c) mx = fmaxf(mx, s[c]);
+            const float mnew = fmaxf(m, mx * p.c);
+            if (mnew != -INFINITY) {
+              float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+              for (int c = 0; c < 64; c += 2) {
+                acc0 += ex2(fmaf(s[c], p.c, -mnew));
+                acc1 += ex2(fmaf(s[c + 1], p.c, -mnew));
+              }
+              z = z * ex2(m - mnew) + (acc0 + acc1);
+              m = mnew;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ctl + C_SEMPTY + 8 * b);
+      }
+      // ---- publish this job's row statistics ----
+      if (p.g == 1) {
+        const int xb = k & 1;
+        const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_XEMPTY + 8 * xb, ((k >> 1) & 1) ^ 1));
+        ok = got;
+        if (got) {
+          xstat[xb * TILE + lrow] = make_float2(m, z);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ctl + C_XFULL + 8 * xb);
+        }
+      } else {
+        p.part[((size_t)j * p.g + xg) * TILE + lrow] = make_float2(m, z);
+        __threadfence();
+        named_bar(2, 128);
+        if (lrow == 0) *last_flag = (atomicAdd(&p.arrive[j], 1) == p.g - 1);
+        named_bar(2, 128);
+        if (*last_flag) {
+          __threadfence();
+          float M = -INFINITY, Z = 0.f;
+          for (int r = 0; r < p.g; ++r) {
+            const float2 o = __ldcg(p.part + ((size_t)j * p.g + r) * TILE + lrow);
+            const float Mn = fmaxf(M, o.x);
+            if (Mn != -INFINITY) Z = Z * ex2(M - Mn) + o.y * ex2(o.x - Mn);
+            M = Mn;
+          }
+          p.fin[(size_t)j * TILE + lrow] = make_float2(M, Z);
+          __threadfence();
+          named_bar(2, 128);
+          if (lrow == 0) atomicExch(&p.ready[j], 1);
+        }
+      }
+    }
+  } else {
+    // ------------------- pass 2: votes (one thread per key) -------------------
+    const int quarter = warp & 3;
+    const int lkey = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const int t2 = threadIdx.x - 192;  // 0..127 within warpgroup 1
+    volatile int *go = reinterpret_cast<volatile int *>(ctrl + C_GO);
+    int it2 = 0;
+    bool ok = true;
+    for (int k = 0; k < njobs; ++k) {
+      const int j = gamma + k * p.ngroups;
+      const Job J = job_geo(p, j, xg);
+      const int n = J.t1 - J.t0;
+      // statistics of this job -> per-row offsets
+      float M = 0.f, Z = 0.f;
+      if (p.g == 1) {
+        const int xb = k & 1;
+        const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_XFULL + 8 * xb, (k >> 1) & 1));
+        ok = got;
+        if (got) {
+          const float2 o = xstat[xb * TILE + t2];
+          M = o.x;
+          Z = o.y;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ctl + C_XEMPTY + 8 * xb);
+        }
+      } else {
+        if (t2 == 0) {
+          bool fine = ok && !ab.raised();
+          if (fine && !spin_flag_bounded(&p.ready[j], p.status, p.timeout)) {
+            ab.raise();
+            fine = false;
+          }
+          *go = fine ? 1 : 0;
+        }
+        named_bar(3, 128);
+        ok = ok && (*go != 0);
+        const float2 o = __ldcg(p.fin + (size_t)j * TILE + t2);
+        M = o.x;
+        Z = o.y;
+      }
+      const bool rvalid = t2 < J.nrows;
+      off[t2] = (rvalid && Z > 0.f) ? M + lg2(Z) : INFINITY;
+      rowpos[t2] = rvalid ? p.L - p.Wq + (J.rho0 + t2) % p.Wq : -1;
+      named_bar(3, 128);
+      for (int i = 0; i < n; ++i, ++it2) {
+        const int b = 2 + (it2 & 1);
+        const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_SFULL + 8 * b, (it2 >> 1) & 1));
+        ok = got;
+        if (!got) continue;
+        tc_fence_after();
+        const int key = (J.t1 - 1 - i) * TILE + lkey;
+        const bool kfull = key <= J.pmin;
+        float v0 = 0.f, v1 = 0.f;
+        for (int c0 = 0; c0 < J.rpad; c0 += 32) {
+          if (J.rpad - c0 >= 32) {
+            float s[32];
+            tmem_ld32(tmem + lane_base + (uint32_t)(b * 128 + c0), s);
+            tmem_wait_ld();
+            if (kfull) {
+#pragma unroll
+              for (int c = 0; c < 32; c += 2) {
+                v0 += ex2(fmaf(s[c], p.c, -off[c0 + c]));
+                v1 += ex2(fmaf(s[c + 1], p.c, -off[c0 + c + 1]));
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const float e = ex2(fmaf(s[c], p.c, -off[c0 + c]));
+                v0 += (key <= rowpos[c0 + c]) ? e : 0.f;
+              }
+            }
+          } else {
+            float s[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)(b * 128 + c0), s);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const float e = ex2(fmaf(s[c], p.c, -off[c0 + c]));
+              v0 += (kfull || key <= rowpos[c0 + c]) ? e : 0.f;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ctl + C_SEMPTY + 8 * b);
+        if (key < J.kend) {
+          float *dst = p.votes + (size_t)J.u * p.L + key;
+          if (p.atomic_votes)
+            atomicAdd(dst, v0 + v1);
+          else
+            *dst = v0 + v1;
+        }
+      }
+      named_bar(3, 128);  // everyone done with off/rowpos of this job
+    }
+  }
+
+  // ---------------------------------- teardown ----------------------------------
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+bool g_attr_done[2][64];
+
+// Group size: a divisor of the grid so each CTA of a job gets at least one tile and, if
+// possible, at most ~10 (the pass-2 re-read of the keys of all concurrent chunks must
+// fit in L2).  Cost model: rounds of jobs x (tiles per CTA + exchange overhead).
+int choose_group(int min_nkt, int max_nkt, long long jobs, int P) {
+  int best = 1;
+  double best_cost = 1e300;
+  for (int g = 1; g <= P; ++g) {
+    if (P % g || g > min_nkt) continue;
+    const int tpc = (max_nkt + g - 1) / g;
+    const long long ngroups = P / g;
+    const long long rounds = (jobs + ngroups - 1) / ngroups;
+    double cost = (double)rounds * (tpc + (g > 1 ? 0.5 : 0.0));
+    if (tpc > 10) cost *= 1.0 + 0.08 * (tpc - 10);
+    if (cost < best_cost) { best_cost = cost; best = g; }
+  }
+  return best;
+}
+
+}  // namespace
+
+WindowVotePlan plan_window_vote(int units, int L, int R, int Wq, int num_sms) {
+  WindowVotePlan pl;
+  pl.row_tiles = (R + TILE - 1) / TILE;
+  pl.jobs = units * pl.row_tiles;
+  pl.min_nkt = 1 << 30;
+  pl.max_nkt = 0;
+  for (int rt = 0; rt < pl.row_tiles; ++rt) {  // key tiles of each row tile
+    const int nrows = (R - rt * TILE) < TILE ? R - rt * TILE : TILE;
+    const int r0 = (rt * TILE) % Wq;
+    const bool wraps = r0 + nrows > Wq;
+    const int rmax = wraps ? Wq - 1 : r0 + nrows - 1;
+    const int nkt = (L - Wq + rmax + 1 + TILE - 1) / TILE;
+    if (nkt < pl.min_nkt) pl.min_nkt = nkt;
+    if (nkt > pl.max_nkt) pl.max_nkt = nkt;
+  }
+  pl.g = choose_group(pl.min_nkt, pl.max_nkt, pl.jobs, num_sms);
+  pl.ngroups = num_sms / pl.g;
+  size_t b = 0;
+  if (pl.g > 1) {
+    b += (size_t)pl.jobs * pl.g * TILE * sizeof(float2);  // part
+    b += (size_t)pl.jobs * TILE * sizeof(float2);         // fin
+    b += 2 * (size_t)pl.jobs * sizeof(int);               // arrive, ready
+  }
+  pl.ws_bytes = (b + 255) & ~(size_t)255;
+  return pl;
+}
+
+cudaError_t launch_window_vote(const Ctx &c, const WindowVoteArgs &a) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int di = a.D == 128 ? 1 : 0;
+  const void *fn = a.D == 128 ? (const void *)window_vote_kernel<128>
+                              : (const void *)window_vote_kernel<64>;
+  const int smem = a.D == 128 ? Geo<128>::SMEM : Geo<64>::SMEM;
+  if (dev < 64 && !g_attr_done[di][dev]) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    g_attr_done[di][dev] = true;
+  }
+  CUtensorMap tq, tk;
+  if (!encode_rows_map(&tq, a.q, (uint64_t)a.units * a.R, a.D, TILE)) return cudaErrorInvalidValue;
+  if (!encode_rows_map(&tk, a.k, (uint64_t)a.units * a.L, a.D, TILE)) return cudaErrorInvalidValue;
+
+  const WindowVotePlan pl = plan_window_vote(a.units, a.L, a.R, a.Wq, c.num_sms);
+  int blocks_per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, fn, NTHREADS, smem);
+  if (e != cudaSuccess) return e;
+  if (blocks_per_sm != 1) return cudaErrorInvalidConfiguration;
+  WVP p;
+  p.L = a.L;
+  p.R = a.R;
+  p.Wq = a.Wq;
+  p.row_tiles = pl.row_tiles;
+  p.jobs = pl.jobs;
+  p.g = pl.g;
+  p.ngroups = pl.ngroups;
+  p.c = (float)(1.4426950408889634 / sqrt((double)a.D));
+  p.votes = a.votes;
+  p.atomic_votes = p.row_tiles > 1;
+  uint8_t *w = reinterpret_cast<uint8_t *>(a.ws);
+  const size_t jobs = (size_t)p.jobs;
+  p.part = reinterpret_cast<float2 *>(w);
+  p.fin = p.part + jobs * p.g * TILE;
+  p.arrive = reinterpret_cast<int *>(p.fin + jobs * TILE);
+  p.ready = p.arrive + jobs;
+  p.status = c.status;
+  p.timeout = c.timeout_ns;
+  const int P = c.num_sms;  // one persistent CTA per SM
+
+  if (p.g > 1) {
+    e = cudaMemsetAsync(p.arrive, 0, 2 * jobs * sizeof(int), c.stream);
+    if (e != cudaSuccess) return e;
+  }
+  if (p.atomic_votes) {
+    e = cudaMemsetAsync(a.votes, 0, (size_t)a.units * a.L * sizeof(float), c.stream);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (a.D == 128) return cudaLaunchKernelEx(&cfg, window_vote_kernel<128>, tq, tk, p);
+  return cudaLaunchKernelEx(&cfg, window_vote_kernel<64>, tq, tk, p);
+}
+
+}  // namespace kvc

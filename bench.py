@@ -1,0 +1,442 @@
+"""Benchmark of the SnapKV hot path on the Mistral-7B-shaped workload.
+
+Workload (synthetic, seeded; the articles' model/dataset workloads are not available):
+batch 2, 32 layers, 32 query / 8 KV heads, head dim 128, prompt 16384 bf16 tokens with
+1% planted hot spans per head, observation window 32, max-pool 7, budget 1024; then
+256 decode steps.  One step = SnapKV compression of all 32 layers (one library call)
+followed by 256 decode steps, each one call that appends the step's K/V to the compact
+cache of all 32 layers and attends over it.
+
+Printed JSON (rank 0): value = prefix tokens compressed per second (B * L / compression
+time); decode_attn = decode-attention HBM GB/s (algorithmic bytes / time) and its
+fraction of the measured HBM peak; roofline of the dominant kernel (decode attention)
+and of the window-score kernel; e2e through the same API with host buffers; the fp64
+oracle as CPU baseline.  --impl reference times the oracle itself.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefix tokens/s compressed & decode-attn HBM GB/s (% of roofline), 1 GB300"
+UNIT = "prefix tokens/s"
+
+# Mistral-7B-shaped workload (--layers / --decode-steps shrink it for profiling only)
+B, LY, HQ, HKV, D, L, W, P, KB, STEPS = 2, 32, 32, 8, 128, 16384, 32, 7, 1024, 256
+G = HQ // HKV
+
+
+def set_size(layers, steps):
+    global LY, STEPS, CAP, UNITS
+    LY, STEPS = layers, steps
+    CAP = KB + STEPS
+    UNITS = LY * B * HKV
+
+
+set_size(LY, STEPS)
+
+
+def compress_bytes():
+    """Algorithmic bytes of one compression of all layers: window queries and keys read
+    once, fp32 votes written and read once, kept K/V rows read and written, positions."""
+    per = (HQ * W * D * 2 + HKV * L * D * 2 + 8 * HKV * (L - W) + 8 * HKV * KB * D + 4 * HKV * KB)
+    return per * LY * B
+
+
+def window_vote_bytes():
+    """Algorithmic bytes of the window-score/vote kernel: Q_win and K read once, votes written."""
+    return (HQ * W * D * 2 + HKV * L * D * 2 + 4 * HKV * L) * LY * B
+
+
+def decode_bytes(n):
+    """Algorithmic bytes of one decode step over n cached rows per unit (all layers): K and
+    V rows read, q read, out written, the appended K/V row written."""
+    return LY * B * (4 * HKV * n * D + 4 * HQ * D + 4 * HKV * D)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j.get("bf16_tflops", 1897.3)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle on a bounded sample of the same workload
+# ------------------------------------------------------------------------------------
+
+def oracle_sample(units_sampled, decode_units, decode_steps, seed):
+    """Times the oracle on `units_sampled` (layer, batch, KV head) units of the workload
+    (votes, pool, top-k, gather) and on decode attention for `decode_units` units over
+    `decode_steps` steps.  Returns (compress s per unit, decode s per unit-step)."""
+    import numpy as np
+    import torch
+
+    import workloads as WL
+    from oracle import attention as OA
+    from oracle import snapkv as OS
+
+    w = WL.MISTRAL
+    import dataclasses
+    w1 = dataclasses.replace(w, layers=1, batch=1)
+    x = WL.snapkv_prompt(w1, seed, "cpu")
+    Q = x["Q_win"].float().numpy().astype(np.float64)
+    K = x["K"].float().numpy().astype(np.float64)
+    V = x["V"].float().numpy().astype(np.float64)
+    t0 = time.perf_counter()
+    kept = []
+    for u in range(units_sampled):
+        h = u % HKV
+        pos, kc, vc, _ = OS.compress_unit(Q[0, 0, h * G:(h + 1) * G], K[0, 0, h], V[0, 0, h], W, P, KB)
+        kept.append((kc, vc))
+    t_c = (time.perf_counter() - t0) / units_sampled
+    rng = np.random.default_rng(seed)
+    t0 = time.perf_counter()
+    for u in range(decode_units):
+        kc, vc = kept[u % len(kept)]
+        kc, vc = kc.copy(), vc.copy()
+        for s in range(decode_steps):
+            q = rng.standard_normal((G, D))
+            kc = np.concatenate([kc, rng.standard_normal((1, D))])
+            vc = np.concatenate([vc, rng.standard_normal((1, D))])
+            OA.attend_group(q, kc, vc)
+    t_d = (time.perf_counter() - t0) / max(1, decode_units * decode_steps)
+    return t_c, t_d
+
+
+def cpu_baseline(units_sampled=128, decode_units=8, decode_steps=128):
+    """Runs oracle_sample single-threaded in a child process (BLAS pinned to 1 thread)."""
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = ("import sys, json; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.oracle_sample(%d, %d, %d, 1002)))"
+            % (ROOT, units_sampled, decode_units, decode_steps))
+    t0 = time.perf_counter()
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    wall = time.perf_counter() - t0
+    if r.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "error": r.stderr.strip().splitlines()[-1] if r.stderr else "failed"}
+    t_c, t_d = json.loads(r.stdout.strip().splitlines()[-1])
+    compress_s = t_c * UNITS
+    decode_s = t_d * UNITS * STEPS
+    return {"value": B * L / compress_s, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": ("%d of %d (layer,batch,kv-head) units compressed, %d units x %d decode steps; "
+                       "scaled by units" % (units_sampled, UNITS, decode_units, decode_steps)),
+            "compress_s_full_workload": compress_s, "decode_ms_per_token_full_workload": 1e3 * decode_s / STEPS,
+            "sample_wall_s": wall}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    steps, warm = args.steps, args.warmup
+    # each step: one oracle unit compression (bounded sample), scaled to the workload
+    import numpy as np  # noqa: F401
+    times = []
+    for i in range(warm + steps):
+        t_c, _ = oracle_sample(1, 0, 0, 1002 + i)
+        if i >= warm:
+            times.append(t_c)
+    per_unit = statistics.median(times)
+    value = B * L / (per_unit * UNITS)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": steps, "warmup": warm, "ms_per_step": 1e3 * per_unit * UNITS,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "1 (layer,batch,kv-head) unit per step, scaled by %d units" % UNITS},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict():
+    full = LY == 32 and STEPS == 256
+    return {"workload": "mistral7b-b2-L16384-gqa32x8-d128-w32-p7-kb1024-decode256" if full else
+            "PROFILING SUBSET (not a bench line): mistral7b-shaped, %d layers, %d decode steps" % (LY, STEPS),
+            "batch": B, "layers": LY, "q_heads": HQ, "kv_heads": HKV, "head_dim": D,
+            "prompt_len": L, "window": W, "pool_kernel": P, "budget": KB, "decode_steps": STEPS,
+            "l2": "inputs larger than L2 (K/V 4.3 GB, compact caches 0.34 GB)"}
+
+
+# ------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import attention_score_kv_snapkv_gb300 as kvc
+    import workloads as WL
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    hbm_peak, tf_peak, peak_kind = peaks()
+
+    w = WL.MISTRAL
+    x = WL.snapkv_prompt(w, WL.seed_of(2, rank), dev, layers=LY)
+    Q, K, V = x["Q_win"], x["K"], x["V"]
+    dec = [WL.decode_token(w, s, WL.seed_of(2, 100 + rank), dev, layers=LY) for s in range(STEPS)]
+    kc = torch.empty((LY, B, HKV, CAP, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    pos = torch.empty((LY, B, HKV, CAP), dtype=torch.int32, device=dev)
+    nv = torch.empty((LY, B, HKV), dtype=torch.int32, device=dev)
+    outs = torch.empty((LY, B, HQ, D), dtype=torch.bfloat16, device=dev)
+
+    def compress():
+        kvc.snapkv_compress(Q, K, V, keep_window=W, pool_kernel=P, budget=KB, cap=CAP, k_out=kc,
+                            v_out=vc, pos_out=pos, n_valid_out=nv)
+
+    def decode(s):
+        q, kn, vn = dec[s]
+        kvc.compressed_decode_attn(q, kc, vc, n_valid=nv, k_new=kn, v_new=vn, pos=pos,
+                                   new_pos=L + s, out=outs)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(record):
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        compress()
+        e1.record(stream)
+        dec_ev = []
+        for s in range(STEPS):
+            a, b = ev(), ev()
+            a.record(stream)
+            decode(s)
+            b.record(stream)
+            dec_ev.append((a, b))
+        if record is not None:
+            record.append(((e0, e1), dec_ev))
+
+    for _ in range(args.warmup):
+        step(None)
+    torch.cuda.synchronize()
+    status = kvc.kvc_device_status()
+    clocks = ClockSampler(dev.index)
+    recs = []
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_all0, t_all1 = ev(), ev()
+    t_all0.record(stream)
+    for _ in range(args.steps):
+        step(recs)
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if ws > 1:
+        dist.barrier()
+    status |= kvc.kvc_device_status()
+    total_ms = t_all0.elapsed_time(t_all1)
+    comp_ms = [c[0].elapsed_time(c[1]) for c, _ in recs]
+    dec_ms = [[a.elapsed_time(b) for a, b in d] for _, d in recs]
+    comp_avg = sum(comp_ms) / len(comp_ms)
+    dec_avg_step = sum(sum(d) for d in dec_ms) / len(dec_ms)          # 256 decode calls
+    dec_bytes_step = sum(decode_bytes(KB + s + 1) for s in range(STEPS))
+    if ws > 1:
+        t = torch.tensor([total_ms, comp_avg, dec_avg_step], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, comp_avg, dec_avg_step = (float(v) for v in t.cpu())
+
+    # e2e: the same API with host (pinned) inputs; H2D of the prompt tensors and of every
+    # decode step's q/k/v, D2H of the final attention output and the cache sizes
+    e2e = None
+    if rank == 0 or ws > 1:
+        hQ, hK, hV = (t.cpu().pin_memory() for t in (Q, K, V))
+        hdec = [tuple(t.cpu().pin_memory() for t in d) for d in dec]
+        hout = torch.empty(outs.shape, dtype=outs.dtype).pin_memory()
+        hnv = torch.empty(nv.shape, dtype=nv.dtype).pin_memory()
+        dq, dk, dvv = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+        ddec = [tuple(torch.empty_like(t) for t in d) for d in dec]
+        h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hV)) + \
+            sum(t.numel() * t.element_size() for d in hdec for t in d)
+        d2h = hout.numel() * hout.element_size() + hnv.numel() * hnv.element_size()
+
+        def e2e_step(rec):
+            a, b, c = ev(), ev(), ev()
+            a.record(stream)
+            dq.copy_(hQ, non_blocking=True)
+            dk.copy_(hK, non_blocking=True)
+            dvv.copy_(hV, non_blocking=True)
+            kvc.snapkv_compress(dq, dk, dvv, keep_window=W, pool_kernel=P, budget=KB, cap=CAP,
+                                k_out=kc, v_out=vc, pos_out=pos, n_valid_out=nv)
+            hnv.copy_(nv, non_blocking=True)
+            b.record(stream)
+            for s in range(STEPS):
+                for dst, src in zip(ddec[s], hdec[s]):
+                    dst.copy_(src, non_blocking=True)
+                q, kn, vn = ddec[s]
+                kvc.compressed_decode_attn(q, kc, vc, n_valid=nv, k_new=kn, v_new=vn, pos=pos,
+                                           new_pos=L + s, out=outs)
+            hout.copy_(outs, non_blocking=True)
+            c.record(stream)
+            if rec is not None:
+                rec.append((a, b, c))
+
+        e2e_step(None)
+        torch.cuda.synchronize()
+        erec = []
+        for _ in range(max(1, min(args.steps, 3))):
+            e2e_step(erec)
+        torch.cuda.synchronize()
+        comp_e2e = statistics.median(a.elapsed_time(b) for a, b, c in erec)
+        all_e2e = statistics.median(a.elapsed_time(c) for a, b, c in erec)
+        e2e = {"value": ws * B * L / (comp_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": all_e2e,
+               "note": "prefix tokens / (H2D of Q_win,K,V + compression + D2H of n_valid); "
+                       "ms_per_step adds 256 decode steps with per-step H2D of q,k,v"}
+
+    dec_gbs = dec_bytes_step / (dec_avg_step / 1e3) / 1e9
+    dec_call_ms = dec_avg_step / STEPS
+    wv_bytes = window_vote_bytes()
+    line = {
+        "metric": METRIC,
+        "value": ws * B * L / (comp_avg / 1e3),
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 in, fp32 accumulate",
+        "data": "synthetic (seeded N(0,1) bf16, planted hot spans)",
+        "config": config_dict(),
+        "compress_ms": comp_avg,
+        "decode_attn": {"GBps": dec_gbs, "frac_of_hbm_peak": dec_gbs / hbm_peak,
+                        "peak_GBps": hbm_peak, "peak_kind": peak_kind,
+                        "frac_of_nominal_8TBps": dec_gbs / 8000.0,
+                        "ms_per_token_all_layers": dec_call_ms,
+                        "launch": "one kernel per decode step covers all %d layers (append fused)" % LY},
+        "roofline": {"kernel": "decode_kernel (compressed_decode_attn, %d layers per launch)" % LY,
+                     "bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": dec_gbs / hbm_peak, "traffic": None,
+                     "peak_kind": peak_kind + " burst copy"},
+        "roofline_compress": {"kernel": "snapkv_compress (window vote + pool/top-k + gather)",
+                              "bound": "hbm", "achieved": compress_bytes() / (comp_avg / 1e3) / 1e9,
+                              "peak": hbm_peak, "unit": "GB/s",
+                              "frac": compress_bytes() / (comp_avg / 1e3) / 1e9 / hbm_peak,
+                              "algorithmic_bytes": compress_bytes()},
+        "gpu_launches": args.steps * (3 + STEPS),
+        "device_status": status,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=32, help="profiling only: fewer layers")
+    ap.add_argument("--decode-steps", type=int, default=256, help="profiling only")
+    args = ap.parse_args()
+    set_size(args.layers, args.decode_steps)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[v] = "1"  # the oracle runs on one core (set before numpy loads)
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

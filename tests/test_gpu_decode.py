@@ -1,0 +1,110 @@
+"""GPU parity of compressed_decode_attn (split-K decode over a compact cache, with and
+without the fused append) against fp64 attention of the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as OA
+from parity import assert_outputs_close, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def rand_cache(Ly, B, Hq, Hkv, D, cap, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((Ly, B, Hq, D), generator=g).to(torch.bfloat16)
+    kc = torch.randn((Ly, B, Hkv, cap, D), generator=g).to(torch.bfloat16)
+    vc = torch.randn((Ly, B, Hkv, cap, D), generator=g).to(torch.bfloat16)
+    return q, kc, vc
+
+
+def oracle_decode(q, kc, vc, n):
+    """q [Ly,B,Hq,D], caches [Ly,B,Hkv,cap,D], n [Ly,B,Hkv] -> [Ly,B,Hq,D] (fp64)."""
+    qh, kh, vh = f64(q), f64(kc), f64(vc)
+    Ly, B, Hq, D = qh.shape
+    Hkv = kh.shape[2]
+    G = Hq // Hkv
+    out = np.zeros_like(qh)
+    for ly in range(Ly):
+        for b in range(B):
+            for h in range(Hkv):
+                m = int(n[ly, b, h])
+                if m == 0:
+                    continue
+                out[ly, b, h * G:(h + 1) * G] = OA.attend_group(qh[ly, b, h * G:(h + 1) * G],
+                                                                kh[ly, b, h, :m], vh[ly, b, h, :m])
+    return out
+
+
+SHAPES = [  # Ly, B, Hq, Hkv, D, cap
+    (1, 2, 8, 2, 128, 300),
+    (2, 1, 4, 4, 64, 129),
+    (1, 1, 32, 8, 128, 1280),
+    (1, 3, 16, 2, 128, 700),
+    (1, 1, 2, 2, 128, 64),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_decode_ragged_n_valid(kvc, shape):
+    Ly, B, Hq, Hkv, D, cap = shape
+    q, kc, vc = rand_cache(Ly, B, Hq, Hkv, D, cap, seed=cap + Hq)
+    g = torch.Generator().manual_seed(7)
+    n = torch.randint(0, cap + 1, (Ly, B, Hkv), generator=g, dtype=torch.int32)
+    n.view(-1)[0] = cap
+    n.view(-1)[-1] = 1 if n.numel() > 1 else cap
+    dev = torch.device("cuda")
+    out = kvc.compressed_decode_attn(q.to(dev), kc.to(dev), vc.to(dev), n_valid=n.to(dev))
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    assert_outputs_close(f64(out), oracle_decode(q, kc, vc, n.numpy()))
+
+
+def test_decode_uniform_n_and_zero_rows(kvc):
+    q, kc, vc = rand_cache(1, 2, 8, 2, 128, 256, seed=3)
+    dev = torch.device("cuda")
+    for n in (0, 1, 63, 64, 65, 256):
+        out = kvc.compressed_decode_attn(q.to(dev), kc.to(dev), vc.to(dev), n_uniform=n)
+        ref = oracle_decode(q, kc, vc, np.full((1, 2, 2), n))
+        assert_outputs_close(f64(out), ref, "n=%d" % n)
+        if n == 0:
+            assert float(out.abs().max()) == 0.0
+
+
+def test_decode_append_then_attend(kvc):
+    Ly, B, Hq, Hkv, D, cap = 1, 2, 8, 2, 128, 200
+    q, kc, vc = rand_cache(Ly, B, Hq, Hkv, D, cap, seed=11)
+    g = torch.Generator().manual_seed(12)
+    kn = torch.randn((Ly, B, Hkv, D), generator=g).to(torch.bfloat16)
+    vn = torch.randn((Ly, B, Hkv, D), generator=g).to(torch.bfloat16)
+    n0 = torch.tensor([[[10, 199], [0, 150]]], dtype=torch.int32)
+    dev = torch.device("cuda")
+    kcd, vcd, nd = kc.to(dev), vc.to(dev), n0.to(dev)
+    pos = torch.full((Ly, B, Hkv, cap), -1, dtype=torch.int32, device=dev)
+    out = kvc.compressed_decode_attn(q.to(dev), kcd, vcd, n_valid=nd, k_new=kn.to(dev),
+                                     v_new=vn.to(dev), pos=pos, new_pos=12345)
+    torch.cuda.synchronize()
+    kc2, vc2 = kc.clone(), vc.clone()
+    for b in range(B):
+        for h in range(Hkv):
+            kc2[0, b, h, n0[0, b, h]] = kn[0, b, h]
+            vc2[0, b, h, n0[0, b, h]] = vn[0, b, h]
+    assert torch.equal(nd.cpu(), n0 + 1)
+    assert torch.equal(kcd.cpu(), kc2) and torch.equal(vcd.cpu(), vc2)
+    assert int(pos[0, 0, 1, 199]) == 12345
+    assert_outputs_close(f64(out), oracle_decode(q, kc2, vc2, (n0 + 1).numpy()))
+    # the unit that is now full drops the next token and flags it
+    out = kvc.compressed_decode_attn(q.to(dev), kcd, vcd, n_valid=nd, k_new=kn.to(dev),
+                                     v_new=vn.to(dev))
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() & kvc.DEV_CACHE_FULL
+    assert int(nd[0, 0, 1]) == cap
+
+
+def test_decode_repeated_calls_reuse_workspace(kvc):
+    q, kc, vc = rand_cache(1, 1, 32, 8, 128, 1280, seed=21)
+    dev = torch.device("cuda")
+    args = (q.to(dev), kc.to(dev), vc.to(dev))
+    outs = [kvc.compressed_decode_attn(*args, n_uniform=1100).clone() for _ in range(3)]
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])

@@ -100,18 +100,22 @@ def hot_positions(w, gen, device):
     """
     Ly, B, H = w.layers, w.batch, w.kv_heads
     n_cand = w.prompt_len - w.window
+    if n_cand < w.span_len or w.spans_per_head == 0:
+        return torch.zeros((Ly, B, H, 0), dtype=torch.int64, device=device)
     if w.span_len == 1:
         keys = torch.rand((Ly * B * H, n_cand), generator=gen, device=device)
-        pos = keys.argsort(dim=1)[:, : w.spans_per_head].sort(dim=1).values
-        return pos.reshape(Ly, B, H, w.spans_per_head)
+        n = min(w.spans_per_head, n_cand)
+        pos = keys.argsort(dim=1)[:, :n].sort(dim=1).values
+        return pos.reshape(Ly, B, H, n)
     block = 2 * w.span_len
     n_blocks = n_cand // block
+    spans = min(w.spans_per_head, n_blocks)
     keys = torch.rand((Ly * B * H, n_blocks), generator=gen, device=device)
-    blocks = keys.argsort(dim=1)[:, : w.spans_per_head].sort(dim=1).values
+    blocks = keys.argsort(dim=1)[:, :spans].sort(dim=1).values
     off = torch.randint(0, w.span_len + 1, blocks.shape, generator=gen, device=device)
     start = blocks * block + off                                 # [units, spans]
     pos = start.unsqueeze(-1) + torch.arange(w.span_len, device=device)
-    return pos.reshape(Ly, B, H, w.spans_per_head * w.span_len)
+    return pos.reshape(Ly, B, H, spans * w.span_len)
 
 
 def snapkv_prompt(w, seed, device, layers=None, full_queries=False):
