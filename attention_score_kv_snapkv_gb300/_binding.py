@@ -70,6 +70,8 @@ _SIGS = {
     "compressed_decode_attn_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(DecodeParams)]),
     "compressed_decode_attn": (ctypes.c_int, [ctypes.POINTER(DecodeParams), _P, _P, _P, _P, _P, _P,
                                               _P, _P, _P, ctypes.c_size_t, _P]),
+    "compressed_decode_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(DecodeParams), _P, _P, _P, _P,
+                                                      _P, _P, _P, _P, _P]),
     "h2o_prefill_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(H2OParams), ctypes.c_int32]),
     "h2o_prefill": (ctypes.c_int, [ctypes.POINTER(H2OParams), ctypes.c_int32, _P, _P, _P,
                                    ctypes.POINTER(H2OStateC), _P, ctypes.c_size_t, _P]),
@@ -261,6 +263,37 @@ def compressed_decode_attn(q, k_cache, v_cache, *, n_valid=None, n_uniform=None,
                                         _ptr(k_cache), _ptr(v_cache), _ptr(pos), _ptr(n_valid),
                                         _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
     _check(code, "compressed_decode_attn")
+    return out
+
+
+def compressed_decode_attn_noalloc(q, k_cache, v_cache, *, n_valid=None, n_uniform=None,
+                                   k_new=None, v_new=None, pos=None, new_pos=0, out=None,
+                                   stream=None):
+    """compressed_decode_attn without a workspace: the library's fixed 8 MiB device
+    scratch array holds the split-K partials (for callers that cannot allocate)."""
+    bf = torch.bfloat16
+    _need(q, "q", bf)
+    _need(k_cache, "k_cache", bf)
+    _need(v_cache, "v_cache", bf, k_cache.shape)
+    Ly, B, Hkv, cap, D = k_cache.shape
+    if n_valid is not None:
+        _need(n_valid, "n_valid", torch.int32, (Ly, B, Hkv))
+    elif n_uniform is None:
+        raise ValueError("give n_valid or n_uniform")
+    if k_new is not None:
+        _need(k_new, "k_new", bf, (Ly, B, Hkv, D))
+        _need(v_new, "v_new", bf, (Ly, B, Hkv, D))
+    if pos is not None:
+        _need(pos, "pos", torch.int32, (Ly, B, Hkv, cap))
+    if out is None:
+        raise ValueError("out must be given: this entry point allocates nothing")
+    _need(out, "out", bf, q.shape)
+    p = decode_params(q, k_cache, 0 if n_uniform is None else n_uniform, new_pos)
+    code = lib().compressed_decode_attn_noalloc(ctypes.byref(p), _ptr(q), _ptr(k_new),
+                                                _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                                _ptr(pos), _ptr(n_valid), _ptr(out),
+                                                _stream(stream))
+    _check(code, "compressed_decode_attn_noalloc")
     return out
 
 

@@ -169,6 +169,23 @@ kvc_status compressed_decode_attn(const kvc_decode_params *p, const void *q, con
                                   int32_t *n_valid, void *out, void *workspace,
                                   size_t workspace_bytes, kvc_stream_t stream);
 
+/* The same decode step for callers that cannot give the library a device workspace:
+ * no counterpart in the articles; it exists for serving engines that own all device
+ * memory through their own pool and pass only the step's tensors to the attention call
+ * (they have no allocator to hand over, and a cudaMalloc mid-step would synchronise
+ * the device).  The split-K scratch lives in a fixed 8 MiB device array inside the
+ * library (held on every GPU that loads it until the process exits); nothing is
+ * allocated.  Arguments and results are those of compressed_decode_attn without the
+ * workspace.  A call needing more scratch than 8 MiB (see
+ * compressed_decode_attn_workspace_bytes) returns KVC_ERR_WORKSPACE and launches
+ * nothing.  The first call on a device looks up the array's device address (with that
+ * device current) and should come before any stream capture.  Each call clears the
+ * counters it uses; calls that overlap on the GPU share the array and race. */
+kvc_status compressed_decode_attn_noalloc(const kvc_decode_params *p, const void *q,
+                                          const void *k_new, const void *v_new, void *k_cache,
+                                          void *v_cache, int32_t *pos, int32_t *n_valid,
+                                          void *out, kvc_stream_t stream);
+
 /* ------------------------------------------------------------------------------ */
 /* H2O heavy-hitter + recent-window cache ([H2O] 何を残すのか, 処理の流れ).          */
 /* ------------------------------------------------------------------------------ */
