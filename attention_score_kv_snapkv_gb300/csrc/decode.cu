@@ -7,17 +7,27 @@
 // unit's finishing CTA writes it to the cache, its position and the new n_valid).
 //
 // Design (sm_103a, HBM-bound: every cached K/V byte is read once):
-// * split-K over the rows: CTA (split s, unit u) covers rows [s*C, (s+1)*C) in tiles of
-//   64 rows; warp 0 streams K and V tiles into a 3-stage shared-memory ring with TMA
-//   (128-byte swizzle, one mbarrier per stage), warps 1-4 compute;
-// * logits: two threads per row (half a head-dim each, conflict-free reads of the
-//   swizzled tile), q in shared memory pre-scaled by log2(e)/sqrt(D), fp32 FMA;
-// * online softmax per warp (16 rows per tile), P.V with lanes over the head dim;
-// * the four warps' states merge in shared memory; with several splits the partial
-//   (m, l, o) goes to the workspace and the last CTA of the unit (atomic counter, no
-//   waiting) merges all splits and writes the bf16 output, resetting the counter.
-//   The counters live in a fixed 256 KB header of the workspace (one int per unit, at
-//   most 65535 units) that is zero between calls, whatever the shapes of the calls.
+// * persistent stream-K: all units' 64-row tile slots form one sequence that is split
+//   evenly over a grid of resident CTAs (two per SM), so every CTA streams the same
+//   number of tiles; a CTA's range covers segments of one or more units.  Warp 0
+//   streams each segment's K tiles and then its V tiles through one continuous 4-stage
+//   shared-memory ring with TMA (128-byte swizzle, one mbarrier pair per stage), so the
+//   next segment's loads overlap the current segment's epilogue; warps 1-4 compute.
+// * K phase: eight threads per row, each owning the same 8 or 16 head dims of every row
+//   (conflict-free reads of the swizzled tile); the thread's slice of q, pre-scaled by
+//   log2(e)/sqrt(D), lives in registers (a bulk copy brings each unit's q to shared
+//   memory ahead of time); packed fp32x2 FMA; a transpose-reduce over the 8 lanes
+//   leaves one head's logit per lane; the logits of the chunk go to shared memory.
+// * one block reduction per chunk gives each head's maximum and normaliser; the logits
+//   become exp2(s - max) in place (chunks of a long segment are merged with a running
+//   maximum, rescaling the sums kept in registers).
+// * V phase: lanes over the head dim, each warp over 16 rows of a tile, packed FMA
+//   with the stored probabilities.  Rows at or past n are never touched.
+// * the four warps' sums merge in shared memory; a unit covered by one segment is
+//   written directly, otherwise each segment's (max, normaliser, o) goes to the
+//   workspace and the last CTA to finish one of the unit's segments (atomic counter,
+//   no waiting) merges them and writes the bf16 output, resetting the counter.  The counters live in a fixed 256 KB header of the workspace (one int per
+//   unit, at most 65535 units) that is zero between calls, whatever the call shapes.
 #include <math.h>
 
 #include "kvc_internal.cuh"
@@ -26,7 +36,7 @@ namespace kvc {
 namespace {
 
 constexpr int ROWS = 64;     // rows per tile
-constexpr int NST = 3;       // ring depth
+constexpr int NST = 4;       // ring depth (K or V tiles)
 constexpr int NCW = 4;       // compute warps
 constexpr int NTH = 32 * (NCW + 1);
 
@@ -34,14 +44,18 @@ template <int D, int G>
 struct DGeo {
   static constexpr int KB = D / 64;
   static constexpr int KBLK = ROWS * 128;        // bytes of one k-block of a tile
-  static constexpr int TB = KB * KBLK;           // bytes of one K (or V) tile
-  static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = NST * TB;
-  static constexpr int OFF_Q = 2 * NST * TB;     // fp32 q [G][D]
-  static constexpr int OFF_RED = OFF_Q + G * D * 4;  // fp32 [NCW][G][D + 2]
-  static constexpr int OFF_BAR = OFF_RED + NCW * G * (D + 2) * 4;
+  static constexpr int TB = KB * KBLK;           // bytes of one K or V tile
+  static constexpr int CMAX = 8192 / G;          // rows of one chunk (logits <= 32 KB)
+  static constexpr int QB = G * D * 2;           // bytes of one unit's q (bf16)
+  static constexpr int OFF_RING = 0;
+  static constexpr int OFF_LOG = NST * TB;                   // fp32 [CMAX][G]
+  static constexpr int OFF_QB = OFF_LOG + CMAX * G * 4;      // bf16 [2][G][D]
+  static constexpr int OFF_RED = OFF_QB + 2 * QB;            // fp32 [NCW][G][D]
+  static constexpr int OFF_ST = OFF_RED + NCW * G * D * 4;   // fp32 [NCW][G]
+  static constexpr int OFF_BAR = OFF_ST + NCW * G * 4 + 64;
   static constexpr int SMEM = OFF_BAR + 128 + 1024;
-  static constexpr int DV = D / 32;              // head-dim elements per lane in P.V
+  static constexpr int DV = D / 32;              // head-dim elements per lane in the V phase
+  static constexpr int NCT = D / 64;             // 16-byte chunks per thread in the K phase
 };
 
 struct DecP {
@@ -52,14 +66,36 @@ struct DecP {
   __nv_bfloat16 *kc, *vc;  // the caches [U, cap, D] (append writes one row)
   int32_t *pos;            // [U, cap] or null
   int new_pos;
-  int n_uniform, cap, chunk, splits;
+  int n_uniform, cap;
+  int units, tiles_per_unit;  // tile slots of 64 rows per unit (for n <= cap)
   __nv_bfloat16 *out;
-  float2 *part_ml;         // [U][S][G]
-  float *part_o;           // [U][S][G][D]
+  float2 *part_ml;         // [U][T][G] per-segment (max, normaliser)
+  float *part_o;           // [U][T][G][D] per-segment unnormalised o
   int *cnt;                // [U]
   uint32_t *status;
   unsigned long long timeout;
 };
+
+// packed fp32x2 helpers: a 64-bit register holds two fp32 lanes
+__device__ __forceinline__ unsigned long long pk(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 upk(unsigned long long v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+// d += a * b, lane-wise on two fp32 values
+__device__ __forceinline__ void ffma2(unsigned long long &d, unsigned long long a,
+                                      unsigned long long b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+// the two bf16 of a packed word as a fp32x2 pair
+__device__ __forceinline__ unsigned long long bf2(uint32_t w) {
+  return pk(bf_lo(w), bf_hi(w));
+}
 
 // Writes 16-byte chunk e of the appended K/V row into the cache; chunk 0's thread also
 // records the position and the new row count.
@@ -74,6 +110,60 @@ __device__ __forceinline__ void append_row(const DecP &p, int u, int arow, int n
   }
 }
 
+// Patches the appended row `arr` of a K or V tile in shared memory (threads 0..D/8-1).
+template <int D>
+__device__ __forceinline__ void patch_row(uint8_t *tile, const __nv_bfloat16 *src_row, int arr,
+                                          int t) {
+  constexpr int KBLK = ROWS * 128;
+  if (t < D / 8) {
+    const int kb = t >> 3, ci = t & 7;
+    uint8_t *dst = tile + kb * KBLK + arr * 128 + ((ci ^ (arr & 7)) << 4);
+    *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src_row + t * 8);
+  }
+}
+
+// Balanced split of `total` tile slots over P CTAs: CTA b owns [first(b), first(b+1)).
+__device__ __forceinline__ int slot_first(int b, int Q, int R) { return b * Q + min(b, R); }
+__device__ __forceinline__ int slot_owner(int slot, int Q, int R) {
+  return slot < R * (Q + 1) ? slot / (Q + 1) : R + (slot - R * (Q + 1)) / Q;
+}
+
+// Geometry of the segment of unit u that CTA b owns.
+struct Seg {
+  int r0, r1;      // rows [r0, r1) of the unit (r1 <= n), possibly empty
+  int arow;        // appended row of the unit, -1 if none
+  int n_old;       // rows before the append
+  int nseg, iseg;  // segments of the unit and this one's index among them
+};
+
+__device__ __forceinline__ Seg seg_geo(const DecP &p, int u, int b, int s0, int s1, int T, int Q,
+                                       int R, bool report) {
+  Seg g;
+  int n = p.n_valid ? p.n_valid[u] : p.n_uniform;
+  if (n > p.cap || n < 0) {
+    if (report) set_status(p.status, KVC_DEV_BAD_STATE);
+    n = n < 0 ? 0 : p.cap;
+  }
+  g.n_old = n;
+  g.arow = -1;
+  if (p.k_new) {
+    if (n < p.cap) {
+      g.arow = n;
+      n = n + 1;
+    } else if (report && slot_owner(u * T, Q, R) == b) {
+      set_status(p.status, KVC_DEV_CACHE_FULL);
+    }
+  }
+  const int t_lo = max(s0, u * T) - u * T, t_hi = min(s1, (u + 1) * T) - u * T;
+  g.r0 = t_lo * ROWS;
+  g.r1 = min(t_hi * ROWS, n);
+  if (g.r1 < g.r0) g.r1 = g.r0;
+  const int b0 = slot_owner(u * T, Q, R), b1 = slot_owner(u * T + T - 1, Q, R);
+  g.nseg = b1 - b0 + 1;
+  g.iseg = b - b0;
+  return g;
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(NTH) decode_kernel(const __grid_constant__ CUtensorMap tk,
                                                      const __grid_constant__ CUtensorMap tv,
@@ -83,34 +173,20 @@ __global__ void __launch_bounds__(NTH) decode_kernel(const __grid_constant__ CUt
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
-  float *qs = reinterpret_cast<float *>(smem + Gm::OFF_Q);
+  float *slog = reinterpret_cast<float *>(smem + Gm::OFF_LOG);  // [row][G]
   float *red = reinterpret_cast<float *>(smem + Gm::OFF_RED);
-  const uint32_t bar = sb + Gm::OFF_BAR;  // full[NST] at +0, empty[NST] at +32
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Gm::OFF_BAR + 64);
-  volatile int *last_flag = reinterpret_cast<volatile int *>(smem + Gm::OFF_BAR + 68);
+  float *wst = reinterpret_cast<float *>(smem + Gm::OFF_ST);    // [NCW][G] per-warp partials
+  // barriers: full[NST] at +0, empty[NST] at +32, qfull[2] at +64, qempty[2] at +80
+  const uint32_t bar = sb + Gm::OFF_BAR;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Gm::OFF_BAR + 96);
+  volatile int *last_flag = reinterpret_cast<volatile int *>(smem + Gm::OFF_BAR + 100);
 
-  const int u = blockIdx.y, s = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Abort ab{abort_flag, p.status, p.timeout};
-
-  int n = p.n_valid ? p.n_valid[u] : p.n_uniform;
-  if (n > p.cap || n < 0) {
-    if (threadIdx.x == 0) set_status(p.status, KVC_DEV_BAD_STATE);
-    n = n < 0 ? 0 : p.cap;
-  }
-  const int n_old = n;
-  int arow = -1;  // row of the appended token, -1 if none
-  if (p.k_new) {
-    if (n < p.cap) {
-      arow = n;
-      n = n + 1;
-    } else if (s == 0 && threadIdx.x == 0) {
-      set_status(p.status, KVC_DEV_CACHE_FULL);
-    }
-  }
-  const int r_begin = s * p.chunk;
-  const int r_end = min(n, r_begin + p.chunk);
-  const int ntiles = r_end > r_begin ? (r_end - r_begin + ROWS - 1) / ROWS : 0;
+  const int T = p.tiles_per_unit, P = gridDim.x, b = blockIdx.x;
+  const int total = p.units * T, Q = total / P, R = total % P;
+  const int s0 = slot_first(b, Q, R), s1 = slot_first(b + 1, Q, R);
+  const int u_first = s0 / T, u_last = s1 > s0 ? (s1 - 1) / T : u_first - 1;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -118,225 +194,351 @@ __global__ void __launch_bounds__(NTH) decode_kernel(const __grid_constant__ CUt
       mbar_init(bar + 8 * i, 1);
       mbar_init(bar + 32 + 8 * i, NCW);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar + 64 + 8 * i, 1);
+      mbar_init(bar + 80 + 8 * i, NCW);
+    }
     fence_mbar_init();
   }
   __syncthreads();
 
   if (warp == 0) {
-    // ---------------------------- TMA producer ----------------------------
-    if (lane == 0 && ntiles > 0) {
+    // ------ TMA producer: per segment its q, then per sub-chunk K tiles, V tiles ------
+    if (lane == 0) {
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      int i = 0;
-      for (; i < ntiles; ++i) {
-        const int st = i % NST, use = i / NST;
-        if (!ab.wait(bar + 32 + 8 * st, (use & 1) ^ 1)) break;
-        mbar_arrive_expect_tx(bar + 8 * st, 2 * Gm::TB);
-        const int row = u * p.cap + r_begin + i * ROWS;
-        for (int kb = 0; kb < Gm::KB; ++kb) {
-          tma_load_2d(sb + Gm::OFF_K + st * Gm::TB + kb * Gm::KBLK, &tk, kb * 64, row, bar + 8 * st);
-          tma_load_2d(sb + Gm::OFF_V + st * Gm::TB + kb * Gm::KBLK, &tv, kb * 64, row, bar + 8 * st);
+      int it = 0, k = 0;
+      bool ok = true;
+      for (int u = u_first; u <= u_last && ok; ++u, ++k) {
+        const Seg g = seg_geo(p, u, b, s0, s1, T, Q, R, false);
+        const int qb = k & 1;
+        if (!ab.wait(bar + 80 + 8 * qb, ((k >> 1) & 1) ^ 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar + 64 + 8 * qb, Gm::QB);
+        bulk_load(sb + Gm::OFF_QB + qb * Gm::QB, p.q + (size_t)u * G * D, Gm::QB, bar + 64 + 8 * qb);
+        for (int c0 = g.r0; c0 < g.r1 && ok; c0 += Gm::CMAX) {
+          const int ntiles = (min(g.r1, c0 + Gm::CMAX) - c0 + ROWS - 1) / ROWS;
+          for (int i = 0; i < 2 * ntiles; ++i, ++it) {
+            const int st = it % NST, use = it / NST;
+            if (!ab.wait(bar + 32 + 8 * st, (use & 1) ^ 1)) { ok = false; break; }
+            mbar_arrive_expect_tx(bar + 8 * st, Gm::TB);
+            const int tt = i < ntiles ? i : i - ntiles;
+            const int row = u * p.cap + c0 + tt * ROWS;
+            const CUtensorMap *map = i < ntiles ? &tk : &tv;
+            for (int kb = 0; kb < Gm::KB; ++kb)
+              tma_load_2d(sb + Gm::OFF_RING + st * Gm::TB + kb * Gm::KBLK, map, kb * 64, row,
+                          bar + 8 * st);
+          }
         }
       }
       for (int st = 0; st < NST; ++st) {  // drain
-        const int cnt = i / NST + (st < i % NST ? 1 : 0);
+        const int cnt = it / NST + (st < it % NST ? 1 : 0);
         if (cnt > 0) mbar_wait_bounded(bar + 8 * st, (cnt - 1) & 1, p.timeout);
       }
+      for (int qb = 0; qb < 2; ++qb) {
+        const int cnt = k / 2 + (qb < k % 2 ? 1 : 0);
+        if (cnt > 0) mbar_wait_bounded(bar + 64 + 8 * qb, (cnt - 1) & 1, p.timeout);
+      }
     }
-  } else {
-    // ------------------------------ compute ------------------------------
-    const int cw = warp - 1;                 // 0..3
-    const int t = threadIdx.x - 32;          // 0..127
-    // q (bf16) -> fp32 pre-scaled
-    for (int e = t; e < G * D; e += 128)
-      qs[e] = __bfloat162float(p.q[(size_t)u * G * D + e]) * p.c;
-    named_bar(1, 128);
+    return;
+  }
 
-    const int r = t >> 1;        // row of the tile for the logit phase
-    const int h = t & 1;         // which half of the head dim
-    constexpr int NCH = D / 16;  // 16-byte chunks per half row
-    float m[G], l[G], o[G][Gm::DV];
+  // ------------------------------ compute warps ------------------------------
+  const int cw = warp - 1;         // 0..3
+  const int t = threadIdx.x - 32;  // 0..127
+  const int rg = lane >> 3;        // K phase: row of the warp's group of 4 rows
+  const int sl = lane & 7;         // K phase: the thread's head-dim slice
+  constexpr int DV = Gm::DV;
+  constexpr int NCT = Gm::NCT;
+  int it = 0, k = 0;
+  bool ok = true;
+  for (int u = u_first; u <= u_last; ++u, ++k) {
+    const Seg sg = seg_geo(p, u, b, s0, s1, T, Q, R, t == 0);
+    // q slice of this thread: chunks sl (+8) of every head, fp32 pairs, pre-scaled
+    unsigned long long qr[G][NCT][4];
+    {
+      const int qb = k & 1;
+      const bool got = __all_sync(0xffffffffu, ok && ab.wait(bar + 64 + 8 * qb, (k >> 1) & 1));
+      ok = got;
+      const uint8_t *qsm = smem + Gm::OFF_QB + qb * Gm::QB;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int c = 0; c < NCT; ++c) {
+          const uint4 w = got ? *reinterpret_cast<const uint4 *>(qsm + (g * D + (sl + 8 * c) * 8) * 2)
+                              : make_uint4(0, 0, 0, 0);
+          qr[g][c][0] = pk(bf_lo(w.x) * p.c, bf_hi(w.x) * p.c);
+          qr[g][c][1] = pk(bf_lo(w.y) * p.c, bf_hi(w.y) * p.c);
+          qr[g][c][2] = pk(bf_lo(w.z) * p.c, bf_hi(w.z) * p.c);
+          qr[g][c][3] = pk(bf_lo(w.w) * p.c, bf_hi(w.w) * p.c);
+        }
+      __syncwarp();
+      if (got && lane == 0) mbar_arrive(bar + 80 + 8 * qb);
+    }
+    float m_run[G], l_run[G];
+    unsigned long long o2[G][DV / 2];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      m[g] = -INFINITY;
-      l[g] = 0.f;
+      m_run[g] = -INFINITY;
+      l_run[g] = 0.f;
 #pragma unroll
-      for (int d = 0; d < Gm::DV; ++d) o[g][d] = 0.f;
+      for (int d = 0; d < DV / 2; ++d) o2[g][d] = 0ull;
     }
-    bool ok = true;
-    for (int i = 0; i < ntiles; ++i) {
-      const int st = i % NST;
-      const bool got = __all_sync(0xffffffffu, ok && ab.wait(bar + 8 * st, (i / NST) & 1));
-      ok = got;
-      const uint8_t *ktp = smem + Gm::OFF_K + st * Gm::TB;
-      const uint8_t *vtp = smem + Gm::OFF_V + st * Gm::TB;
-      const int arr = arow - (r_begin + i * ROWS);  // the appended row in this tile?
-      const bool patched = arow >= 0 && arr >= 0 && arr < ROWS;  // same for the whole CTA
-      if (patched) {
-        // every compute thread reaches this barrier, whether or not its wait succeeded
-        if (got && t < 2 * (D / 8)) {
-          const int which = t / (D / 8), cidx = t % (D / 8);
-          const int kb = cidx >> 3, ci = cidx & 7;
-          uint8_t *dst = smem + (which ? Gm::OFF_V : Gm::OFF_K) + st * Gm::TB + kb * Gm::KBLK +
-                         arr * 128 + ((ci ^ (arr & 7)) << 4);
-          const __nv_bfloat16 *src = (which ? p.v_new : p.k_new) + (size_t)u * D + cidx * 8;
-          *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+    for (int c0 = sg.r0; c0 < sg.r1; c0 += Gm::CMAX) {
+      const int nrows = min(sg.r1, c0 + Gm::CMAX) - c0;
+      const int ntiles = (nrows + ROWS - 1) / ROWS;
+      const int arow_local = sg.arow - c0;
+      // ---- K phase: logits of the sub-chunk's rows (8 threads per row) ----
+      for (int i = 0; i < ntiles; ++i) {
+        const int j = it + i, st = j % NST;
+        const bool got = __all_sync(0xffffffffu, ok && ab.wait(bar + 8 * st, (j / NST) & 1));
+        ok = got;
+        uint8_t *tile = smem + Gm::OFF_RING + st * Gm::TB;
+        const int arr = arow_local - i * ROWS;
+        const bool patched = sg.arow >= 0 && arr >= 0 && arr < ROWS;  // same for the CTA
+        if (patched) {  // every compute thread reaches this barrier
+          if (got) patch_row<D>(tile, p.k_new + (size_t)u * D, arr, t);
+          named_bar(1, 128);
+        }
+        if (got) {
+#pragma unroll
+          for (int pass = 0; pass < ROWS / 16; ++pass) {
+            const int r = pass * 16 + cw * 4 + rg;  // row of the tile
+            unsigned long long acc[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) acc[g] = 0ull;
+#pragma unroll
+            for (int c = 0; c < NCT; ++c) {
+              // chunk sl + 8c: k-block c, slot sl of the row (8 lanes of a row hit 8 slots)
+              const uint4 w = *reinterpret_cast<const uint4 *>(tile + c * Gm::KBLK + r * 128 +
+                                                                ((sl ^ (r & 7)) << 4));
+              const unsigned long long k01 = bf2(w.x), k23 = bf2(w.y), k45 = bf2(w.z),
+                                       k67 = bf2(w.w);
+#pragma unroll
+              for (int g = 0; g < G; ++g) {
+                ffma2(acc[g], qr[g][c][0], k01);
+                ffma2(acc[g], qr[g][c][1], k23);
+                ffma2(acc[g], qr[g][c][2], k45);
+                ffma2(acc[g], qr[g][c][3], k67);
+              }
+            }
+            // transpose-reduce over the row's 8 lanes: each split level halves the heads a
+            // lane keeps; afterwards lane bits (from bit 2 down) name the head it holds
+            float v[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const float2 a = upk(acc[g]);
+              v[g] = a.x + a.y;
+            }
+            int head = 0;
+#pragma unroll
+            for (int lvl = 4, nv = G; lvl >= 1; lvl >>= 1) {
+              if (nv >= 2) {
+                const bool upper = (lane & lvl) != 0;
+#pragma unroll
+                for (int x = 0; x < G / 2; ++x) {
+                  if (x < nv / 2) {
+                    const float send = upper ? v[x] : v[x + nv / 2];
+                    const float keep = upper ? v[x + nv / 2] : v[x];
+                    v[x] = keep + __shfl_xor_sync(0xffffffffu, send, lvl);
+                  }
+                }
+                if (upper) head += nv / 2;
+                nv /= 2;
+              } else {
+                v[0] += __shfl_xor_sync(0xffffffffu, v[0], lvl);
+              }
+            }
+            const int row = i * ROWS + r;
+            if ((lane & (8 / G - 1)) == 0 && row < nrows) slog[row * G + head] = v[0];
+          }
+          if (patched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar + 32 + 8 * st);
+        }
+      }
+      named_bar(1, 128);
+      // ---- sub-chunk max; new running max; p = exp2(s - max) in place; sums ----
+      float mnew[G], f[G];
+      {
+        float mx[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) mx[g] = -INFINITY;
+        for (int r = t; r < nrows; r += 128)
+#pragma unroll
+          for (int g = 0; g < G; ++g) mx[g] = fmaxf(mx[g], slog[r * G + g]);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], o));
+          if (lane == 0) wst[cw * G + g] = mx[g];
         }
         named_bar(1, 128);
-      }
-      if (!got) continue;
-      // ---- logits: this thread's half row ----
-      float acc[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) acc[g] = 0.f;
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        const int cc = (D == 128) ? ((c + 4 * h) & 7) : c;      // rotation: conflict-free
-        const int chunk = h * NCH + cc;                          // 16-byte chunk in the row
-        const int kb = chunk >> 3, ci = chunk & 7;
-        const uint4 w = *reinterpret_cast<const uint4 *>(ktp + kb * Gm::KBLK + r * 128 +
-                                                          ((ci ^ (r & 7)) << 4));
-        const float kf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
-                             bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
-        const int d0 = chunk * 8;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float4 qa = *reinterpret_cast<const float4 *>(qs + g * D + d0);
-          const float4 qb = *reinterpret_cast<const float4 *>(qs + g * D + d0 + 4);
-          acc[g] = fmaf(qa.x, kf[0], acc[g]);
-          acc[g] = fmaf(qa.y, kf[1], acc[g]);
-          acc[g] = fmaf(qa.z, kf[2], acc[g]);
-          acc[g] = fmaf(qa.w, kf[3], acc[g]);
-          acc[g] = fmaf(qb.x, kf[4], acc[g]);
-          acc[g] = fmaf(qb.y, kf[5], acc[g]);
-          acc[g] = fmaf(qb.z, kf[6], acc[g]);
-          acc[g] = fmaf(qb.w, kf[7], acc[g]);
+          float m2 = m_run[g];
+#pragma unroll
+          for (int w2 = 0; w2 < NCW; ++w2) m2 = fmaxf(m2, wst[w2 * G + g]);
+          mnew[g] = m2;
+          f[g] = m_run[g] == -INFINITY ? 0.f : ex2(m_run[g] - m2);  // rescale of earlier sums
+        }
+        float sm[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) sm[g] = 0.f;
+        for (int r = t; r < nrows; r += 128)
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float e = ex2(slog[r * G + g] - mnew[g]);
+            slog[r * G + g] = e;
+            sm[g] += e;
+          }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sm[g] += __shfl_xor_sync(0xffffffffu, sm[g], o);
+        }
+        named_bar(1, 128);  // every warp read the maxima before wst is reused for sums
+        if (lane == 0)
+#pragma unroll
+          for (int g = 0; g < G; ++g) wst[cw * G + g] = sm[g];
+        named_bar(1, 128);  // sums and probabilities visible to all compute warps
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float l2 = 0.f;
+#pragma unroll
+          for (int w2 = 0; w2 < NCW; ++w2) l2 += wst[w2 * G + g];
+          l_run[g] = l_run[g] * f[g] + l2;
+          m_run[g] = mnew[g];
+          const unsigned long long ff = pk(f[g], f[g]);
+#pragma unroll
+          for (int d = 0; d < DV / 2; ++d) {
+            unsigned long long z = 0ull;
+            ffma2(z, o2[g][d], ff);
+            o2[g][d] = z;
+          }
         }
       }
-      const bool rvalid = r_begin + i * ROWS + r < r_end;
-      float pr[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float x = acc[g] + __shfl_xor_sync(0xffffffffu, acc[g], 1);
-        x = rvalid ? x : -INFINITY;
-        float mx = x;
-#pragma unroll
-        for (int o2 = 2; o2 < 32; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
-        const float mnew = fmaxf(m[g], mx);
-        float scale = 1.f, pe = 0.f;
-        if (mnew != -INFINITY) {
-          scale = ex2(m[g] - mnew);
-          pe = ex2(x - mnew);
+      // ---- V phase: o[g] += p[row][g] * v[row], lanes over the head dim ----
+      for (int i = 0; i < ntiles; ++i) {
+        const int j = it + ntiles + i, st = j % NST;
+        const bool got = __all_sync(0xffffffffu, ok && ab.wait(bar + 8 * st, (j / NST) & 1));
+        ok = got;
+        uint8_t *tile = smem + Gm::OFF_RING + st * Gm::TB;
+        const int arr = arow_local - i * ROWS;
+        const bool patched = sg.arow >= 0 && arr >= 0 && arr < ROWS;
+        if (patched) {
+          if (got) patch_row<D>(tile, p.v_new + (size_t)u * D, arr, t);
+          named_bar(1, 128);
         }
-        float ps = (h == 0) ? pe : 0.f;
-#pragma unroll
-        for (int o2 = 1; o2 < 32; o2 <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o2);
-        l[g] = l[g] * scale + ps;
-        m[g] = mnew;
-#pragma unroll
-        for (int d = 0; d < Gm::DV; ++d) o[g][d] *= scale;
-        pr[g] = pe;
-      }
-      // ---- P.V: lanes over the head dim, the warp's 16 rows ----
+        if (got) {
+          const int rmax = min(16, nrows - i * ROWS - cw * 16);  // this warp's rows in the tile
 #pragma unroll 4
-      for (int i2 = 0; i2 < 16; ++i2) {
-        const int rr = cw * 16 + i2;
-        float vf[Gm::DV];
-        if (D == 128) {
-          const int chunk = lane >> 1, kb = chunk >> 3, ci = chunk & 7;
-          const uint2 w = *reinterpret_cast<const uint2 *>(vtp + kb * Gm::KBLK + rr * 128 +
-                                                           ((ci ^ (rr & 7)) << 4) + (lane & 1) * 8);
-          vf[0] = bf_lo(w.x);
-          vf[1] = bf_hi(w.x);
-          vf[2 % Gm::DV] = bf_lo(w.y);
-          vf[3 % Gm::DV] = bf_hi(w.y);
-        } else {
-          const int ci = lane >> 2;
-          const uint32_t w = *reinterpret_cast<const uint32_t *>(vtp + rr * 128 + ((ci ^ (rr & 7)) << 4) +
-                                                                 (lane & 3) * 4);
-          vf[0] = bf_lo(w);
-          vf[1 % Gm::DV] = bf_hi(w);
-        }
+          for (int i2 = 0; i2 < 16; ++i2) {
+            if (i2 >= rmax) break;
+            const int rr = cw * 16 + i2;
+            unsigned long long v01, v23 = 0ull;
+            if (D == 128) {
+              const int chunk = lane >> 1, kb = chunk >> 3, ci = chunk & 7;
+              const uint2 w = *reinterpret_cast<const uint2 *>(
+                  tile + kb * Gm::KBLK + rr * 128 + ((ci ^ (rr & 7)) << 4) + (lane & 1) * 8);
+              v01 = bf2(w.x);
+              v23 = bf2(w.y);
+            } else {
+              const int ci = lane >> 2;
+              const uint32_t w = *reinterpret_cast<const uint32_t *>(
+                  tile + rr * 128 + ((ci ^ (rr & 7)) << 4) + (lane & 3) * 4);
+              v01 = bf2(w);
+            }
+            const float *pr = slog + (i * ROWS + rr) * G;
+            float pv[G];
+            if (G >= 4) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float pv = __shfl_sync(0xffffffffu, pr[g], 2 * i2);
+              for (int g = 0; g < G; g += 4) {
+                const float4 q4 = *reinterpret_cast<const float4 *>(pr + g);
+                pv[g] = q4.x;
+                pv[(g + 1) % G] = q4.y;
+                pv[(g + 2) % G] = q4.z;
+                pv[(g + 3) % G] = q4.w;
+              }
+            } else {
 #pragma unroll
-          for (int d = 0; d < Gm::DV; ++d) o[g][d] = fmaf(pv, vf[d], o[g][d]);
+              for (int g = 0; g < G; ++g) pv[g] = pr[g];
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const unsigned long long pp = pk(pv[g], pv[g]);
+              ffma2(o2[g][0], pp, v01);
+              if (DV == 4) ffma2(o2[g][DV / 2 - 1], pp, v23);
+            }
+          }
+          if (patched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar + 32 + 8 * st);
         }
       }
-      // generic-proxy writes to this stage must be ordered before the next TMA into it
-      if (patched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar + 32 + 8 * st);
+      it += 2 * ntiles;
+      named_bar(1, 128);  // slog and wst of this sub-chunk are done with
     }
-    // ---- merge the four warps ----
-    float *mine = red + cw * G * (D + 2);
+    // ---- merge the four warps' sums of this segment ----
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
+    for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int d = 0; d < Gm::DV; ++d) mine[g * (D + 2) + lane * Gm::DV + d] = o[g][d];
-      if (lane == 0) {
-        mine[g * (D + 2) + D] = m[g];
-        mine[g * (D + 2) + D + 1] = l[g];
+      for (int d = 0; d < DV / 2; ++d) {
+        const float2 v = upk(o2[g][d]);
+        red[(cw * G + g) * D + lane * DV + 2 * d] = v.x;
+        red[(cw * G + g) * D + lane * DV + 2 * d + 1] = v.y;
       }
-    }
     named_bar(1, 128);
-    const bool direct = p.splits == 1;
+    const bool direct = sg.nseg == 1;
     for (int e = t; e < G * D; e += 128) {
       const int g = e / D, d = e - g * D;
-      float M = -INFINITY;
-      for (int w2 = 0; w2 < NCW; ++w2) M = fmaxf(M, red[(w2 * G + g) * (D + 2) + D]);
-      float L = 0.f, O = 0.f;
-      if (M != -INFINITY) {
-        for (int w2 = 0; w2 < NCW; ++w2) {
-          const float* src = red + (w2 * G + g) * (D + 2);
-          const float f = ex2(src[D] - M);
-          L += src[D + 1] * f;
-          O += src[d] * f;
-        }
-      }
+      float O = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < NCW; ++w2) O += red[(w2 * G + g) * D + d];
       if (direct) {
-        p.out[(size_t)u * G * D + e] = __float2bfloat16(L > 0.f ? O / L : 0.f);
-        if (e < D / 8 && arow >= 0) append_row<D>(p, u, arow, n_old, e);
+        p.out[(size_t)u * G * D + e] = __float2bfloat16(l_run[g] > 0.f ? O / l_run[g] : 0.f);
+        if (e < D / 8 && sg.arow >= 0) append_row<D>(p, u, sg.arow, sg.n_old, e);
       } else {
-        p.part_o[(((size_t)u * p.splits + s) * G + g) * D + d] = O;
-        if (d == 0) p.part_ml[((size_t)u * p.splits + s) * G + g] = make_float2(M, L);
+        p.part_o[(((size_t)u * T + sg.iseg) * G + g) * D + d] = O;
+        if (d == 0) p.part_ml[((size_t)u * T + sg.iseg) * G + g] = make_float2(m_run[g], l_run[g]);
       }
     }
     if (!direct) {
       __threadfence();
       named_bar(1, 128);
-      if (t == 0) *last_flag = (atomicAdd(&p.cnt[u], 1) == p.splits - 1);
+      if (t == 0) *last_flag = (atomicAdd(&p.cnt[u], 1) == sg.nseg - 1);
       named_bar(1, 128);
       if (*last_flag) {
         __threadfence();
         for (int e = t; e < G * D; e += 128) {
           const int g = e / D, d = e - g * D;
           float M = -INFINITY;
-          for (int s2 = 0; s2 < p.splits; ++s2)
-            M = fmaxf(M, __ldcg(p.part_ml + ((size_t)u * p.splits + s2) * G + g).x);
+          for (int s2 = 0; s2 < sg.nseg; ++s2)
+            M = fmaxf(M, __ldcg(p.part_ml + ((size_t)u * T + s2) * G + g).x);
           float L = 0.f, O = 0.f;
           if (M != -INFINITY) {
-            for (int s2 = 0; s2 < p.splits; ++s2) {
-              const float2 ml = __ldcg(p.part_ml + ((size_t)u * p.splits + s2) * G + g);
-              const float f = ex2(ml.x - M);
-              L += ml.y * f;
-              O += __ldcg(p.part_o + (((size_t)u * p.splits + s2) * G + g) * D + d) * f;
+            for (int s2 = 0; s2 < sg.nseg; ++s2) {
+              const float2 ml = __ldcg(p.part_ml + ((size_t)u * T + s2) * G + g);
+              if (ml.y <= 0.f) continue;  // an empty segment
+              const float fs = ex2(ml.x - M);
+              L += ml.y * fs;
+              O += __ldcg(p.part_o + (((size_t)u * T + s2) * G + g) * D + d) * fs;
             }
           }
           p.out[(size_t)u * G * D + e] = __float2bfloat16(L > 0.f ? O / L : 0.f);
         }
-        if (arow >= 0)
-          for (int e = t; e < D / 8; e += 128) append_row<D>(p, u, arow, n_old, e);
+        if (sg.arow >= 0)
+          for (int e = t; e < D / 8; e += 128) append_row<D>(p, u, sg.arow, sg.n_old, e);
         if (t == 0) p.cnt[u] = 0;
       }
     }
+    named_bar(1, 128);  // qs, red and last_flag are reused by the next segment
   }
 }
 
 template <int D, int G>
-cudaError_t launch_t(const Ctx &c, const DecodeArgs &a, const DecP &p, dim3 grid) {
+cudaError_t launch_t(const Ctx &c, const DecodeArgs &a, DecP p) {
   static bool attr[64];
+  static int per_sm[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr[dev]) {
@@ -344,32 +546,30 @@ cudaError_t launch_t(const Ctx &c, const DecodeArgs &a, const DecP &p, dim3 grid
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DGeo<D, G>::SMEM);
     if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[dev], decode_kernel<D, G>, NTH,
+                                                      DGeo<D, G>::SMEM);
+    if (e != cudaSuccess) return e;
+    if (per_sm[dev] < 1) return cudaErrorInvalidConfiguration;
     attr[dev] = true;
   }
   CUtensorMap tk, tv;
   if (!encode_rows_map(&tk, a.k_cache, (uint64_t)a.units * a.cap, D, ROWS)) return cudaErrorInvalidValue;
   if (!encode_rows_map(&tv, a.v_cache, (uint64_t)a.units * a.cap, D, ROWS)) return cudaErrorInvalidValue;
-  decode_kernel<D, G><<<grid, NTH, DGeo<D, G>::SMEM, c.stream>>>(tk, tv, p);
+  // persistent grid: every resident CTA slot, but never more CTAs than tile slots
+  const long long slots = (long long)a.units * p.tiles_per_unit;
+  long long grid = (long long)c.num_sms * (dev < 64 ? per_sm[dev] : 1);
+  if (grid > slots) grid = slots;
+  if (grid < 1) grid = 1;
+  decode_kernel<D, G><<<(unsigned)grid, NTH, DGeo<D, G>::SMEM, c.stream>>>(tk, tv, p);
   return cudaGetLastError();
-}
-
-// splits and chunk: enough CTAs to fill the GPU about twice over, chunks of whole tiles
-void plan_splits(int units, int n_max, int num_sms, int *splits, int *chunk) {
-  const int max_splits = n_max > 0 ? (n_max + ROWS - 1) / ROWS : 1;
-  const int target = 4 * num_sms;
-  int S = (target + units - 1) / units;
-  if (S < 1) S = 1;
-  if (S > max_splits) S = max_splits;
-  int C = n_max > 0 ? (n_max + S - 1) / S : ROWS;
-  C = (C + ROWS - 1) / ROWS * ROWS;
-  *chunk = C;
-  *splits = n_max > 0 ? (n_max + C - 1) / C : 1;
 }
 
 }  // namespace
 
 constexpr size_t CNT_HEADER = 65536 * sizeof(int);  // per-unit counters, zero between calls
 
+// Workspace: the counter header, then per unit and segment (at most one segment per
+// tile slot) the partial (max, normaliser) per head and the partial o per head.
 size_t decode_ws_bytes(int units, int G, int D, int cap, int num_sms) {
   const size_t smax = (size_t)(cap > 0 ? (cap + ROWS - 1) / ROWS : 1);
   size_t b = CNT_HEADER;
@@ -381,8 +581,7 @@ size_t decode_ws_bytes(int units, int G, int D, int cap, int num_sms) {
 
 cudaError_t launch_decode(const Ctx &c, const DecodeArgs &a) {
   const int n_max = a.n_valid ? a.cap : a.n_uniform;
-  int splits, chunk;
-  plan_splits(a.units, n_max, c.num_sms, &splits, &chunk);
+  const int T = n_max > 0 ? (n_max + ROWS - 1) / ROWS : 1;  // tile slots per unit
   const size_t smax = (size_t)(a.cap > 0 ? (a.cap + ROWS - 1) / ROWS : 1);
   DecP p;
   p.q = reinterpret_cast<const __nv_bfloat16 *>(a.q);
@@ -396,8 +595,8 @@ cudaError_t launch_decode(const Ctx &c, const DecodeArgs &a) {
   p.new_pos = a.new_pos;
   p.n_uniform = a.n_uniform;
   p.cap = a.cap;
-  p.chunk = chunk;
-  p.splits = splits;
+  p.units = a.units;
+  p.tiles_per_unit = T;
   p.out = reinterpret_cast<__nv_bfloat16 *>(a.out);
   uint8_t *w = reinterpret_cast<uint8_t *>(a.ws);
   p.cnt = reinterpret_cast<int *>(w);
@@ -405,9 +604,8 @@ cudaError_t launch_decode(const Ctx &c, const DecodeArgs &a) {
   p.part_o = reinterpret_cast<float *>(w + CNT_HEADER + (size_t)a.units * smax * a.G * sizeof(float2));
   p.status = c.status;
   p.timeout = c.timeout_ns;
-  const dim3 grid(splits, a.units);
 #define KVC_DEC(DD, GG) \
-  if (a.D == DD && a.G == GG) return launch_t<DD, GG>(c, a, p, grid);
+  if (a.D == DD && a.G == GG) return launch_t<DD, GG>(c, a, p);
   KVC_DEC(128, 1) KVC_DEC(128, 2) KVC_DEC(128, 4) KVC_DEC(128, 8)
   KVC_DEC(64, 1) KVC_DEC(64, 2) KVC_DEC(64, 4) KVC_DEC(64, 8)
 #undef KVC_DEC

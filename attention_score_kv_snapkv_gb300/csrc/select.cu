@@ -70,9 +70,18 @@ __global__ void __launch_bounds__(NT, 1) pool_topk_kernel(const TopkP p) {
     for (int i = tid; i < nb; i += NT) hist[i] = 0;
     __syncthreads();
     const uint32_t prefix = (uint32_t)misc[0];
-    for (int j = tid; j < n; j += NT) {
-      const uint32_t key = kb[j];
-      if ((key & mask_hi) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
+    // warp-aggregated counting: one shared atomic per distinct bin per warp (the first
+    // digit puts most keys into a handful of bins)
+    for (int j0 = warp * 32; j0 < n; j0 += NT) {
+      const int j = j0 + lane;
+      const uint32_t key = j < n ? kb[j] : 0u;
+      const bool valid = j < n && (key & mask_hi) == prefix;
+      const uint32_t vm = __ballot_sync(0xffffffffu, valid);
+      if (valid) {
+        const uint32_t bin = (key >> sh) & (nb - 1);
+        const uint32_t grp = __match_any_sync(vm, bin);
+        if (lane == __ffs(grp) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(grp));
+      }
     }
     __syncthreads();
     if (warp == 0) {

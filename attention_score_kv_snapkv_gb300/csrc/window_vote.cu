@@ -9,19 +9,21 @@
 //   128-key tiles; the tiles are split over a group of g CTAs of a persistent,
 //   cooperatively launched grid (one CTA per SM).
 // * Pass 1, per key tile: S = Q . K^T on the tensor cores (tcgen05.mma, M = 128 query
-//   rows, N = 128 keys, fp32 accumulator in TMEM).  Warpgroup 0 (one thread per row)
-//   keeps each row's running max m and normaliser z (log2 domain).
+//   rows, N = 128 keys, fp32 accumulator in TMEM).  The pass-1 warps (one thread per
+//   row and column half) keep each row's running max m and normaliser z (log2 domain).
 // * Row statistics are combined across the g CTAs of the job through global memory
 //   (the last CTA to arrive combines and publishes; bounded spin for the others).
 // * Pass 2, per key tile: S^T = K . Q^T (M = 128 keys, N = rows rounded up to 16);
-//   warpgroup 1 (one thread per key) sums exp2(s*c - (m + log2 z)) over its rows in
-//   registers -- no cross-lane reduction -- and writes the vote.
+//   the pass-2 warps (one thread per key and row half) sum exp2(s*c - (m + log2 z))
+//   over their rows in registers -- no cross-lane reduction -- and write the vote.
 // * Pass 2 of job k is interleaved with pass 1 of job k+1 (after a lead of two
 //   tiles), so the re-read of job k's keys comes from L2 and the statistics exchange
 //   is hidden behind useful work.
 // * Warp roles: warp 0 = TMA producer (Q tiles double-buffered, K tiles in a 4-stage
-//   ring, 128-byte swizzle), warp 1 = TMEM owner and MMA issuer, warps 2-5 = pass 1,
-//   warps 6-9 = pass 2.  Every wait is bounded (KVC_DEV_TIMEOUT on expiry).
+//   ring, 128-byte swizzle), warp 1 = TMEM owner and MMA issuer, warps 2-9 = pass 1
+//   (two warps per TMEM lane quarter, each on half of the tile's key columns), warps
+//   10-17 = pass 2 (two per lane quarter, each on half of the query rows; the halves
+//   of a key's vote meet in shared memory).  Every wait is bounded (KVC_DEV_TIMEOUT).
 #include <math.h>
 
 #include "kvc_internal.cuh"
@@ -31,7 +33,7 @@ namespace {
 
 constexpr int TILE = 128;       // keys per tile; query rows per job
 constexpr int NSTAGE = 4;       // K tile ring depth
-constexpr int NTHREADS = 320;   // 10 warps
+constexpr int NTHREADS = 576;   // 18 warps: TMA, MMA, 8 pass-1 and 8 pass-2 warps
 constexpr int TMEM_COLS = 512;  // 4 accumulators of 128 fp32 columns
 constexpr int LEAD = 2;         // pass-1 tiles of job k+1 issued before pass 2 of job k
 
@@ -43,7 +45,7 @@ struct Geo {
   static constexpr int OFF_Q = 0;             // 2 Q tiles
   static constexpr int OFF_K = 2 * TILE_BYTES;
   static constexpr int OFF_CTRL = OFF_K + NSTAGE * TILE_BYTES;
-  static constexpr int CTRL_BYTES = 4096;
+  static constexpr int CTRL_BYTES = 8192;
   static constexpr int NEED = OFF_CTRL + CTRL_BYTES + 1024;  // + base alignment slack
   // At least 116 KB so that two CTAs never share an SM: each CTA allocates all 512
   // TMEM columns, and the persistent grid relies on one resident CTA per SM.
@@ -65,7 +67,9 @@ constexpr int C_LAST = 200;
 constexpr int C_XSTAT = 256;    // float2 [2][128]  (2048 B)
 constexpr int C_OFF = 2304;     // float [128]
 constexpr int C_ROWPOS = 2816;  // int [128]
-constexpr int C_GO = 3328;      // int: pass-2 warpgroup may proceed (g > 1)
+constexpr int C_GO = 3328;      // int: pass-2 warps may proceed (g > 1)
+constexpr int C_HSTAT = 3456;   // float2 [2][128]: second column half's row statistics
+constexpr int C_VPART = 5504;   // float [2][128]: second row half's partial votes
 
 struct WVP {
   int L, R, Wq, row_tiles, jobs, g, ngroups;
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int b = 0; b < 4; ++b) {
       mbar_init(ctl + C_SFULL + 8 * b, 1);
-      mbar_init(ctl + C_SEMPTY + 8 * b, 4);
+      mbar_init(ctl + C_SEMPTY + 8 * b, 8);  // the 8 warps of the pass
     }
     fence_mbar_init();
   }
@@ -274,13 +278,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // drain: wait for the completion of the last MMA batch issued
       if (last_bar >= 0) mbar_wait_bounded(ctl + C_SFULL + 8 * last_bar, last_par, p.timeout);
     }
-  } else if (warp < 6) {
-    // ------------------ pass 1: row statistics (one thread per row) ------------------
-    // Control flow (loops, named barriers) is identical for every thread of the
-    // warpgroup; a failed wait only turns the remaining work off (ok = false).
+  } else if (warp < 10) {
+    // --------- pass 1: row statistics (8 warps: TMEM lane quarter x column half) ---------
+    // Control flow (loops, named barriers) is identical for every thread of the pass; a
+    // failed wait only turns the remaining work off (ok = false).
     const int quarter = warp & 3;
+    const int ch = (warp - 2) >> 2;  // which 64 of the tile's 128 key columns
     const int lrow = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    float2 *hstat = reinterpret_cast<float2 *>(ctrl + C_HSTAT);
     int it1 = 0;
     bool ok = true;
     for (int k = 0; k < njobs; ++k) {
@@ -298,77 +304,86 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!got) continue;
         tc_fence_after();
         if (warp_active) {
-          const int kbase = (J.t0 + i) * TILE;
-          const bool full = kbase + TILE - 1 <= prow;
-#pragma unroll 1
-          for (int h = 0; h < 2; ++h) {
-            float s[64];
-            tmem_ld32(tmem + lane_base + (uint32_t)(b * 128 + h * 64), s);
-            tmem_ld32(tmem + lane_base + (uint32_t)(b * 128 + h * 64 + 32), s + 32);
-            tmem_wait_ld();
-            if (!full) {
+          const int kbase = (J.t0 + i) * TILE + ch * 64;
+          float s[64];
+          tmem_ld32(tmem + lane_base + (uint32_t)(b * 128 + ch * 64), s);
+          tmem_ld32(tmem + lane_base + (uint32_t)(b * 128 + ch * 64 + 32), s + 32);
+          tmem_wait_ld();
+          if (kbase + 63 > prow) {
 #pragma unroll
-              for (int c = 0; c < 64; ++c)
-                if (kbase + h * 64 + c > prow) s[c] = -INFINITY;
+            for (int c = 0; c < 64; ++c)
+              if (kbase + c > prow) s[c] = -INFINITY;
+          }
+          float mx0 = s[0], mx1 = s[1];
+#pragma unroll
+          for (int c = 2; c < 64; c += 2) {
+            mx0 = fmaxf(mx0, s[c]);
+            mx1 = fmaxf(mx1, s[c + 1]);
+          }
+          const float mnew = fmaxf(m, fmaxf(mx0, mx1) * p.c);
+          if (mnew != -INFINITY) {
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+              acc0 += ex2(fmaf(s[c], p.c, -mnew));
+              acc1 += ex2(fmaf(s[c + 1], p.c, -mnew));
             }
-            float mx = s[0];
-#pragma unroll
-            for (int c = 1; c < 64; ++c) mx = fmaxf(mx, s[c]);
-            const float mnew = fmaxf(m, mx * p.c);
-            if (mnew != -INFINITY) {
-              float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-              for (int c = 0; c < 64; c += 2) {
-                acc0 += ex2(fmaf(s[c], p.c, -mnew));
-                acc1 += ex2(fmaf(s[c + 1], p.c, -mnew));
-              }
-              z = z * ex2(m - mnew) + (acc0 + acc1);
-              m = mnew;
-            }
+            z = z * ex2(m - mnew) + (acc0 + acc1);
+            m = mnew;
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(ctl + C_SEMPTY + 8 * b);
       }
-      // ---- publish this job's row statistics ----
-      if (p.g == 1) {
-        const int xb = k & 1;
-        const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_XEMPTY + 8 * xb, ((k >> 1) & 1) ^ 1));
-        ok = got;
-        if (got) {
-          xstat[xb * TILE + lrow] = make_float2(m, z);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(ctl + C_XFULL + 8 * xb);
-        }
-      } else {
-        p.part[((size_t)j * p.g + xg) * TILE + lrow] = make_float2(m, z);
-        __threadfence();
-        named_bar(2, 128);
-        if (lrow == 0) *last_flag = (atomicAdd(&p.arrive[j], 1) == p.g - 1);
-        named_bar(2, 128);
-        if (*last_flag) {
-          __threadfence();
-          float M = -INFINITY, Z = 0.f;
-          for (int r = 0; r < p.g; ++r) {
-            const float2 o = __ldcg(p.part + ((size_t)j * p.g + r) * TILE + lrow);
-            const float Mn = fmaxf(M, o.x);
-            if (Mn != -INFINITY) Z = Z * ex2(M - Mn) + o.y * ex2(o.x - Mn);
-            M = Mn;
+      // ---- merge the two column halves, then publish this job's row statistics ----
+      if (ch == 1) hstat[(k & 1) * TILE + lrow] = make_float2(m, z);
+      named_bar(2, 256);
+      if (ch == 0) {
+        const float2 o = hstat[(k & 1) * TILE + lrow];
+        const float mn = fmaxf(m, o.x);
+        if (mn != -INFINITY) z = z * ex2(m - mn) + o.y * ex2(o.x - mn);
+        m = mn;
+        if (p.g == 1) {
+          const int xb = k & 1;
+          const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_XEMPTY + 8 * xb, ((k >> 1) & 1) ^ 1));
+          ok = got;
+          if (got) {
+            xstat[xb * TILE + lrow] = make_float2(m, z);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ctl + C_XFULL + 8 * xb);
           }
-          p.fin[(size_t)j * TILE + lrow] = make_float2(M, Z);
+        } else {
+          p.part[((size_t)j * p.g + xg) * TILE + lrow] = make_float2(m, z);
           __threadfence();
-          named_bar(2, 128);
-          if (lrow == 0) atomicExch(&p.ready[j], 1);
+          named_bar(4, 128);
+          if (lrow == 0) *last_flag = (atomicAdd(&p.arrive[j], 1) == p.g - 1);
+          named_bar(4, 128);
+          if (*last_flag) {
+            __threadfence();
+            float M = -INFINITY, Z = 0.f;
+            for (int r = 0; r < p.g; ++r) {
+              const float2 o2 = __ldcg(p.part + ((size_t)j * p.g + r) * TILE + lrow);
+              const float Mn = fmaxf(M, o2.x);
+              if (Mn != -INFINITY) Z = Z * ex2(M - Mn) + o2.y * ex2(o2.x - Mn);
+              M = Mn;
+            }
+            p.fin[(size_t)j * TILE + lrow] = make_float2(M, Z);
+            __threadfence();
+            named_bar(4, 128);
+            if (lrow == 0) atomicExch(&p.ready[j], 1);
+          }
         }
       }
     }
   } else {
-    // ------------------- pass 2: votes (one thread per key) -------------------
+    // ------------- pass 2: votes (8 warps: TMEM lane quarter (keys) x row half) -------------
     const int quarter = warp & 3;
+    const int rh = (warp - 10) >> 2;  // which half of the job's query rows
     const int lkey = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const int t2 = threadIdx.x - 192;  // 0..127 within warpgroup 1
+    const int t2 = threadIdx.x - 320;  // 0..255; the first 128 own one row each
+    float *vpart = reinterpret_cast<float *>(ctrl + C_VPART);
     volatile int *go = reinterpret_cast<volatile int *>(ctrl + C_GO);
     int it2 = 0;
     bool ok = true;
@@ -376,18 +391,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int j = gamma + k * p.ngroups;
       const Job J = job_geo(p, j, xg);
       const int n = J.t1 - J.t0;
-      // statistics of this job -> per-row offsets
+      // statistics of this job -> per-row offsets (threads 0..127, i.e. the rh == 0 warps)
       float M = 0.f, Z = 0.f;
       if (p.g == 1) {
-        const int xb = k & 1;
-        const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_XFULL + 8 * xb, (k >> 1) & 1));
-        ok = got;
-        if (got) {
-          const float2 o = xstat[xb * TILE + t2];
-          M = o.x;
-          Z = o.y;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(ctl + C_XEMPTY + 8 * xb);
+        if (rh == 0) {
+          const int xb = k & 1;
+          const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_XFULL + 8 * xb, (k >> 1) & 1));
+          ok = got;
+          if (got) {
+            const float2 o = xstat[xb * TILE + t2];
+            M = o.x;
+            Z = o.y;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ctl + C_XEMPTY + 8 * xb);
+          }
         }
       } else {
         if (t2 == 0) {
@@ -398,66 +415,77 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           *go = fine ? 1 : 0;
         }
-        named_bar(3, 128);
+        named_bar(3, 256);
         ok = ok && (*go != 0);
-        const float2 o = __ldcg(p.fin + (size_t)j * TILE + t2);
-        M = o.x;
-        Z = o.y;
+        if (t2 < TILE) {
+          const float2 o = __ldcg(p.fin + (size_t)j * TILE + t2);
+          M = o.x;
+          Z = o.y;
+        }
       }
-      const bool rvalid = t2 < J.nrows;
-      off[t2] = (rvalid && Z > 0.f) ? M + lg2(Z) : INFINITY;
-      rowpos[t2] = rvalid ? p.L - p.Wq + (J.rho0 + t2) % p.Wq : -1;
-      named_bar(3, 128);
+      if (t2 < TILE) {
+        const bool rvalid = t2 < J.nrows;
+        off[t2] = (rvalid && Z > 0.f) ? M + lg2(Z) : INFINITY;
+        rowpos[t2] = rvalid ? p.L - p.Wq + (J.rho0 + t2) % p.Wq : -1;
+      }
+      named_bar(3, 256);
+      const int half = J.rpad >> 1;  // rows per half: a multiple of 8
+      const int r_lo = rh * half;
       for (int i = 0; i < n; ++i, ++it2) {
         const int b = 2 + (it2 & 1);
         const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_SFULL + 8 * b, (it2 >> 1) & 1));
         ok = got;
-        if (!got) continue;
-        tc_fence_after();
         const int key = (J.t1 - 1 - i) * TILE + lkey;
-        const bool kfull = key <= J.pmin;
         float v0 = 0.f, v1 = 0.f;
-        for (int c0 = 0; c0 < J.rpad; c0 += 32) {
-          if (J.rpad - c0 >= 32) {
+        if (got) {
+          tc_fence_after();
+          const bool kfull = key <= J.pmin;
+          for (int c0 = 0; c0 < half;) {
+            const int w = half - c0 >= 32 ? 32 : (half - c0 >= 16 ? 16 : 8);
+            const int r0 = r_lo + c0;
+            const uint32_t ta = tmem + lane_base + (uint32_t)(b * 128 + r0);
             float s[32];
-            tmem_ld32(tmem + lane_base + (uint32_t)(b * 128 + c0), s);
+            if (w == 32) tmem_ld32(ta, s);
+            else if (w == 16) tmem_ld16(ta, s);
+            else tmem_ld8(ta, s);
             tmem_wait_ld();
             if (kfull) {
 #pragma unroll
               for (int c = 0; c < 32; c += 2) {
-                v0 += ex2(fmaf(s[c], p.c, -off[c0 + c]));
-                v1 += ex2(fmaf(s[c + 1], p.c, -off[c0 + c + 1]));
+                if (c < w) {
+                  v0 += ex2(fmaf(s[c], p.c, -off[r0 + c]));
+                  v1 += ex2(fmaf(s[c + 1], p.c, -off[r0 + c + 1]));
+                }
               }
             } else {
 #pragma unroll
               for (int c = 0; c < 32; ++c) {
-                const float e = ex2(fmaf(s[c], p.c, -off[c0 + c]));
-                v0 += (key <= rowpos[c0 + c]) ? e : 0.f;
+                if (c < w) {
+                  const float e = ex2(fmaf(s[c], p.c, -off[r0 + c]));
+                  v0 += (key <= rowpos[r0 + c]) ? e : 0.f;
+                }
               }
             }
-          } else {
-            float s[16];
-            tmem_ld16(tmem + lane_base + (uint32_t)(b * 128 + c0), s);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const float e = ex2(fmaf(s[c], p.c, -off[c0 + c]));
-              v0 += (kfull || key <= rowpos[c0 + c]) ? e : 0.f;
-            }
+            c0 += w;
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ctl + C_SEMPTY + 8 * b);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(ctl + C_SEMPTY + 8 * b);
-        if (key < J.kend) {
+        // the two row halves of this key meet in shared memory (one pair barrier per tile)
+        const int par = it2 & 1;
+        if (rh == 1) vpart[par * TILE + lkey] = v0 + v1;
+        named_bar(8 + quarter, 64);
+        if (rh == 0 && got && key < J.kend) {
+          const float v = v0 + v1 + vpart[par * TILE + lkey];
           float *dst = p.votes + (size_t)J.u * p.L + key;
           if (p.atomic_votes)
-            atomicAdd(dst, v0 + v1);
+            atomicAdd(dst, v);
           else
-            *dst = v0 + v1;
+            *dst = v;
         }
       }
-      named_bar(3, 128);  // everyone done with off/rowpos of this job
+      named_bar(3, 256);  // everyone done with off/rowpos of this job
     }
   }
 

@@ -108,3 +108,18 @@ def test_decode_repeated_calls_reuse_workspace(kvc):
     args = (q.to(dev), kc.to(dev), vc.to(dev))
     outs = [kvc.compressed_decode_attn(*args, n_uniform=1100).clone() for _ in range(3)]
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+def test_rows_past_n_are_never_read_into_the_output(kvc):
+    # stale cache rows past n (here NaN bit patterns) must not reach the output
+    q, kc, vc = rand_cache(1, 2, 8, 2, 128, 300, seed=31)
+    n = torch.tensor([[[130, 257]]], dtype=torch.int32).expand(1, 2, 2).contiguous()
+    kc2, vc2 = kc.clone(), vc.clone()
+    for b in range(2):
+        for h in range(2):
+            kc2[0, b, h, n[0, b, h]:] = float("nan")
+            vc2[0, b, h, n[0, b, h]:] = float("nan")
+    dev = torch.device("cuda")
+    out = kvc.compressed_decode_attn(q.to(dev), kc2.to(dev), vc2.to(dev), n_valid=n.to(dev))
+    assert torch.isfinite(out.float()).all()
+    assert_outputs_close(f64(out), oracle_decode(q, kc, vc, n.numpy()))
