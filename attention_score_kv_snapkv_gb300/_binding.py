@@ -238,7 +238,9 @@ def compressed_decode_attn(q, k_cache, v_cache, *, n_valid=None, n_uniform=None,
                            v_new=None, pos=None, new_pos=0, out=None, workspace_buf=None,
                            stream=None):
     """One decode step: optional append of (k_new, v_new) at n_valid, then attention of
-    q [Ly,B,Hq,D] over the first n rows of the cache [Ly,B,Hkv,cap,D].  Returns out."""
+    q [Ly,B,Hq,D] over the first n rows of the cache [Ly,B,Hkv,cap,D].  With n_valid,
+    n_uniform may give an upper bound on the rows after the append (plans less work).
+    Returns out."""
     bf = torch.bfloat16
     _need(q, "q", bf)
     _need(k_cache, "k_cache", bf)

@@ -8,15 +8,15 @@
 //
 // Design (sm_103a, HBM-bound: every cached K/V byte is read once):
 // * persistent stream-K: all units' 64-row tile slots form one sequence that is split
-//   evenly over a grid of resident CTAs (two per SM), so every CTA streams the same
+//   evenly over a grid of resident CTAs (three per SM), so every CTA streams the same
 //   number of tiles; a CTA's range covers segments of one or more units.  Warp 0
-//   streams each segment's K tiles and then its V tiles through one continuous 4-stage
+//   streams each segment's K tiles and then its V tiles through one continuous 3-stage
 //   shared-memory ring with TMA (128-byte swizzle, one mbarrier pair per stage), so the
 //   next segment's loads overlap the current segment's epilogue; warps 1-4 compute.
-// * K phase: eight threads per row, each owning the same 8 or 16 head dims of every row
-//   (conflict-free reads of the swizzled tile); the thread's slice of q, pre-scaled by
-//   log2(e)/sqrt(D), lives in registers (a bulk copy brings each unit's q to shared
-//   memory ahead of time); packed fp32x2 FMA; a transpose-reduce over the 8 lanes
+// * K phase: D/8 threads per row, each owning one 16-byte chunk (8 head dims) of every
+//   row (conflict-free reads of the swizzled tile); the thread's slice of q, pre-scaled
+//   by log2(e)/sqrt(D), lives in registers (a bulk copy brings each unit's q to shared
+//   memory ahead of time); packed fp32x2 FMA; a transpose-reduce over the row's lanes
 //   leaves one head's logit per lane; the logits of the chunk go to shared memory.
 // * one block reduction per chunk gives each head's maximum and normaliser; the logits
 //   become exp2(s - max) in place (chunks of a long segment are merged with a running
@@ -36,7 +36,7 @@ namespace kvc {
 namespace {
 
 constexpr int ROWS = 64;     // rows per tile
-constexpr int NST = 4;       // ring depth (K or V tiles)
+constexpr int NST = 3;       // ring depth (K or V tiles)
 constexpr int NCW = 4;       // compute warps
 constexpr int NTH = 32 * (NCW + 1);
 
@@ -45,17 +45,18 @@ struct DGeo {
   static constexpr int KB = D / 64;
   static constexpr int KBLK = ROWS * 128;        // bytes of one k-block of a tile
   static constexpr int TB = KB * KBLK;           // bytes of one K or V tile
-  static constexpr int CMAX = 8192 / G;          // rows of one chunk (logits <= 32 KB)
+  static constexpr int CMAX = 4096 / G;          // rows of one chunk (logits = 16 KB)
   static constexpr int QB = G * D * 2;           // bytes of one unit's q (bf16)
   static constexpr int OFF_RING = 0;
-  static constexpr int OFF_LOG = NST * TB;                   // fp32 [CMAX][G]
+  static constexpr int OFF_LOG = NST * TB;                   // fp32 [CMAX][G]; the merge
+                                                             // buffer [NCW][G][D] reuses it
   static constexpr int OFF_QB = OFF_LOG + CMAX * G * 4;      // bf16 [2][G][D]
-  static constexpr int OFF_RED = OFF_QB + 2 * QB;            // fp32 [NCW][G][D]
-  static constexpr int OFF_ST = OFF_RED + NCW * G * D * 4;   // fp32 [NCW][G]
+  static constexpr int OFF_ST = OFF_QB + 2 * QB;             // fp32 [NCW][G]
   static constexpr int OFF_BAR = OFF_ST + NCW * G * 4 + 64;
   static constexpr int SMEM = OFF_BAR + 128 + 1024;
   static constexpr int DV = D / 32;              // head-dim elements per lane in the V phase
-  static constexpr int NCT = D / 64;             // 16-byte chunks per thread in the K phase
+  static constexpr int TPR = D / 8;              // K phase: threads per row, one chunk each
+  static_assert(NCW * G * D * 4 <= CMAX * G * 4, "merge buffer must fit the logit buffer");
 };
 
 struct DecP {
@@ -154,6 +155,9 @@ __device__ __forceinline__ Seg seg_geo(const DecP &p, int u, int b, int s0, int 
       set_status(p.status, KVC_DEV_CACHE_FULL);
     }
   }
+  if (n > T * ROWS) {  // more rows than the planned bound: they are not attended
+    if (report) set_status(p.status, KVC_DEV_BAD_STATE);
+  }
   const int t_lo = max(s0, u * T) - u * T, t_hi = min(s1, (u + 1) * T) - u * T;
   g.r0 = t_lo * ROWS;
   g.r1 = min(t_hi * ROWS, n);
@@ -165,7 +169,7 @@ __device__ __forceinline__ Seg seg_geo(const DecP &p, int u, int b, int s0, int 
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(NTH) decode_kernel(const __grid_constant__ CUtensorMap tk,
+__global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ CUtensorMap tk,
                                                      const __grid_constant__ CUtensorMap tv,
                                                      const DecP p) {
   using Gm = DGeo<D, G>;
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(NTH) decode_kernel(const __grid_constant__ CUt
   uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
   float *slog = reinterpret_cast<float *>(smem + Gm::OFF_LOG);  // [row][G]
-  float *red = reinterpret_cast<float *>(smem + Gm::OFF_RED);
+  float *red = slog;  // merge buffer, used only after a segment's V phase
   float *wst = reinterpret_cast<float *>(smem + Gm::OFF_ST);    // [NCW][G] per-warp partials
   // barriers: full[NST] at +0, empty[NST] at +32, qfull[2] at +64, qempty[2] at +80
   const uint32_t bar = sb + Gm::OFF_BAR;
@@ -245,32 +249,30 @@ __global__ void __launch_bounds__(NTH) decode_kernel(const __grid_constant__ CUt
   // ------------------------------ compute warps ------------------------------
   const int cw = warp - 1;         // 0..3
   const int t = threadIdx.x - 32;  // 0..127
-  const int rg = lane >> 3;        // K phase: row of the warp's group of 4 rows
-  const int sl = lane & 7;         // K phase: the thread's head-dim slice
+  constexpr int TPR = Gm::TPR;
+  const int rg = lane / TPR;       // K phase: row within the warp's group of 32/TPR rows
+  const int sl = lane % TPR;       // K phase: the thread's 16-byte chunk of the row
   constexpr int DV = Gm::DV;
-  constexpr int NCT = Gm::NCT;
   int it = 0, k = 0;
   bool ok = true;
   for (int u = u_first; u <= u_last; ++u, ++k) {
     const Seg sg = seg_geo(p, u, b, s0, s1, T, Q, R, t == 0);
-    // q slice of this thread: chunks sl (+8) of every head, fp32 pairs, pre-scaled
-    unsigned long long qr[G][NCT][4];
+    // q slice of this thread: chunk sl of every head, fp32 pairs, pre-scaled
+    unsigned long long qr[G][4];
     {
       const int qb = k & 1;
       const bool got = __all_sync(0xffffffffu, ok && ab.wait(bar + 64 + 8 * qb, (k >> 1) & 1));
       ok = got;
       const uint8_t *qsm = smem + Gm::OFF_QB + qb * Gm::QB;
 #pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int c = 0; c < NCT; ++c) {
-          const uint4 w = got ? *reinterpret_cast<const uint4 *>(qsm + (g * D + (sl + 8 * c) * 8) * 2)
-                              : make_uint4(0, 0, 0, 0);
-          qr[g][c][0] = pk(bf_lo(w.x) * p.c, bf_hi(w.x) * p.c);
-          qr[g][c][1] = pk(bf_lo(w.y) * p.c, bf_hi(w.y) * p.c);
-          qr[g][c][2] = pk(bf_lo(w.z) * p.c, bf_hi(w.z) * p.c);
-          qr[g][c][3] = pk(bf_lo(w.w) * p.c, bf_hi(w.w) * p.c);
-        }
+      for (int g = 0; g < G; ++g) {
+        const uint4 w = got ? *reinterpret_cast<const uint4 *>(qsm + (g * D + sl * 8) * 2)
+                            : make_uint4(0, 0, 0, 0);
+        qr[g][0] = pk(bf_lo(w.x) * p.c, bf_hi(w.x) * p.c);
+        qr[g][1] = pk(bf_lo(w.y) * p.c, bf_hi(w.y) * p.c);
+        qr[g][2] = pk(bf_lo(w.z) * p.c, bf_hi(w.z) * p.c);
+        qr[g][3] = pk(bf_lo(w.w) * p.c, bf_hi(w.w) * p.c);
+      }
       __syncwarp();
       if (got && lane == 0) mbar_arrive(bar + 80 + 8 * qb);
     }
@@ -300,38 +302,31 @@ __global__ void __launch_bounds__(NTH) decode_kernel(const __grid_constant__ CUt
           named_bar(1, 128);
         }
         if (got) {
-#pragma unroll
-          for (int pass = 0; pass < ROWS / 16; ++pass) {
-            const int r = pass * 16 + cw * 4 + rg;  // row of the tile
-            unsigned long long acc[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) acc[g] = 0ull;
-#pragma unroll
-            for (int c = 0; c < NCT; ++c) {
-              // chunk sl + 8c: k-block c, slot sl of the row (8 lanes of a row hit 8 slots)
-              const uint4 w = *reinterpret_cast<const uint4 *>(tile + c * Gm::KBLK + r * 128 +
-                                                                ((sl ^ (r & 7)) << 4));
-              const unsigned long long k01 = bf2(w.x), k23 = bf2(w.y), k45 = bf2(w.z),
-                                       k67 = bf2(w.w);
-#pragma unroll
-              for (int g = 0; g < G; ++g) {
-                ffma2(acc[g], qr[g][c][0], k01);
-                ffma2(acc[g], qr[g][c][1], k23);
-                ffma2(acc[g], qr[g][c][2], k45);
-                ffma2(acc[g], qr[g][c][3], k67);
-              }
-            }
-            // transpose-reduce over the row's 8 lanes: each split level halves the heads a
-            // lane keeps; afterwards lane bits (from bit 2 down) name the head it holds
+          constexpr int RPW = 32 / TPR;  // rows per warp and pass
+#pragma unroll 2
+          for (int pass = 0; pass < ROWS / (NCW * RPW); ++pass) {
+            const int r = (pass * NCW + cw) * RPW + rg;  // row of the tile
+            // chunk sl: k-block sl / 8, slot sl % 8 (the 8 lanes of a phase hit 8 slots)
+            const uint4 w = *reinterpret_cast<const uint4 *>(
+                tile + (sl >> 3) * Gm::KBLK + r * 128 + (((sl & 7) ^ (r & 7)) << 4));
+            const unsigned long long k01 = bf2(w.x), k23 = bf2(w.y), k45 = bf2(w.z),
+                                     k67 = bf2(w.w);
             float v[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-              const float2 a = upk(acc[g]);
+              unsigned long long acc = 0ull;
+              ffma2(acc, qr[g][0], k01);
+              ffma2(acc, qr[g][1], k23);
+              ffma2(acc, qr[g][2], k45);
+              ffma2(acc, qr[g][3], k67);
+              const float2 a = upk(acc);
               v[g] = a.x + a.y;
             }
+            // transpose-reduce over the row's TPR lanes: each split level halves the heads a
+            // lane keeps; afterwards the lane's high bits name the head it holds
             int head = 0;
 #pragma unroll
-            for (int lvl = 4, nv = G; lvl >= 1; lvl >>= 1) {
+            for (int lvl = TPR / 2, nv = G; lvl >= 1; lvl >>= 1) {
               if (nv >= 2) {
                 const bool upper = (lane & lvl) != 0;
 #pragma unroll
@@ -349,7 +344,8 @@ __global__ void __launch_bounds__(NTH) decode_kernel(const __grid_constant__ CUt
               }
             }
             const int row = i * ROWS + r;
-            if ((lane & (8 / G - 1)) == 0 && row < nrows) slog[row * G + head] = v[0];
+            constexpr int WMASK = TPR / G > 1 ? TPR / G - 1 : 0;
+            if ((lane & WMASK) == 0 && row < nrows) slog[row * G + head] = v[0];
           }
           if (patched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
@@ -511,17 +507,20 @@ __global__ void __launch_bounds__(NTH) decode_kernel(const __grid_constant__ CUt
         __threadfence();
         for (int e = t; e < G * D; e += 128) {
           const int g = e / D, d = e - g * D;
+          // independent loads (batched by unrolling), then the merge
           float M = -INFINITY;
+#pragma unroll 4
           for (int s2 = 0; s2 < sg.nseg; ++s2)
             M = fmaxf(M, __ldcg(p.part_ml + ((size_t)u * T + s2) * G + g).x);
           float L = 0.f, O = 0.f;
           if (M != -INFINITY) {
+#pragma unroll 4
             for (int s2 = 0; s2 < sg.nseg; ++s2) {
               const float2 ml = __ldcg(p.part_ml + ((size_t)u * T + s2) * G + g);
-              if (ml.y <= 0.f) continue;  // an empty segment
-              const float fs = ex2(ml.x - M);
+              const float o = __ldcg(p.part_o + (((size_t)u * T + s2) * G + g) * D + d);
+              const float fs = ml.y > 0.f ? ex2(ml.x - M) : 0.f;  // empty segments add 0
               L += ml.y * fs;
-              O += __ldcg(p.part_o + (((size_t)u * T + s2) * G + g) * D + d) * fs;
+              O += o * fs;
             }
           }
           p.out[(size_t)u * G * D + e] = __float2bfloat16(L > 0.f ? O / L : 0.f);
@@ -580,7 +579,9 @@ size_t decode_ws_bytes(int units, int G, int D, int cap, int num_sms) {
 }
 
 cudaError_t launch_decode(const Ctx &c, const DecodeArgs &a) {
-  const int n_max = a.n_valid ? a.cap : a.n_uniform;
+  // rows per unit to plan for: n_uniform, or with n_valid the caller's bound on the row
+  // count after the append (0: the capacity)
+  const int n_max = a.n_valid ? (a.n_uniform > 0 ? a.n_uniform : a.cap) : a.n_uniform;
   const int T = n_max > 0 ? (n_max + ROWS - 1) / ROWS : 1;  // tile slots per unit
   const size_t smax = (size_t)(a.cap > 0 ? (a.cap + ROWS - 1) / ROWS : 1);
   DecP p;

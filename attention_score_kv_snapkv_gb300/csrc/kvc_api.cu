@@ -300,7 +300,7 @@ kvc_status compressed_decode_attn(const kvc_decode_params *p, const void *q, con
   if (G != 1 && G != 2 && G != 4 && G != 8) return KVC_ERR_SHAPE;
   const long long units = (long long)p->n_layers * p->batch * p->n_kv_heads;
   if (units * p->cap > kMaxRows || units > 65535ll * 32768ll) return KVC_ERR_SHAPE;
-  if (!n_valid && (p->n_uniform < 0 || p->n_uniform > p->cap)) return KVC_ERR_SHAPE;
+  if (p->n_uniform < 0 || p->n_uniform > p->cap) return KVC_ERR_SHAPE;
   if (!q || !k_cache || !v_cache || !out) return KVC_ERR_NULL;
   if ((k_new == nullptr) != (v_new == nullptr)) return KVC_ERR_NULL;
   if (k_new && !n_valid) return KVC_ERR_NULL;

@@ -145,7 +145,10 @@ kvc_status snapkv_compress(const kvc_snapkv_params *p, const void *q_win, const 
 typedef struct {
   int32_t n_layers, batch, n_q_heads, n_kv_heads, head_dim; /* as above */
   int32_t cap;        /* rows per unit in k_cache / v_cache */
-  int32_t n_uniform;  /* entries attended in every unit when n_valid == NULL */
+  int32_t n_uniform;  /* n_valid == NULL: entries attended in every unit.  n_valid given:
+                         0, or an upper bound on every unit's row count after the append
+                         that the work is planned for (rows beyond it are not attended and
+                         raise KVC_DEV_BAD_STATE); 0 plans for the full capacity */
   int32_t new_pos;    /* position recorded in pos[] for an appended token */
 } kvc_decode_params;
 
