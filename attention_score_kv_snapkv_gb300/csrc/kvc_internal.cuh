@@ -121,15 +121,16 @@ struct Abort {
   }
 };
 
-// Spin (bounded) until *flag != 0 with acquire semantics at GPU scope.  Gives up early
+// Spin (bounded) until *ctr >= target with acquire semantics at GPU scope.  Gives up early
 // if another CTA has already flagged a timeout in the status word.
-__device__ __forceinline__ bool spin_flag_bounded(const int *flag, const uint32_t *status,
-                                                  unsigned long long limit_ns) {
+__device__ __forceinline__ bool spin_count_bounded(const int *ctr, int target,
+                                                   const uint32_t *status,
+                                                   unsigned long long limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0; it < (1u << 24); ++it) {
     int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-    if (v != 0) return true;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
     if (*(volatile const uint32_t *)status & KVC_DEV_TIMEOUT) return false;
     if (globaltimer_ns() - t0 > limit_ns) return false;
     __nanosleep(64);

@@ -22,7 +22,7 @@ __global__ void selftest_wait_kernel(uint32_t *status, unsigned long long limit)
   __syncthreads();
   if (threadIdx.x == 0) {
     int result = 0;
-    if (!spin_flag_bounded(&g_never_set, status, limit)) {
+    if (!spin_count_bounded(&g_never_set, 1, status, limit)) {
       set_status(status, KVC_DEV_TIMEOUT);
       result |= 1;
     }

@@ -11,8 +11,10 @@
 // * Pass 1, per key tile: S = Q . K^T on the tensor cores (tcgen05.mma, M = 128 query
 //   rows, N = 128 keys, fp32 accumulator in TMEM).  The pass-1 warps (one thread per
 //   row and column half) keep each row's running max m and normaliser z (log2 domain).
-// * Row statistics are combined across the g CTAs of the job through global memory
-//   (the last CTA to arrive combines and publishes; bounded spin for the others).
+// * Row statistics are combined across the g CTAs of the job through global memory:
+//   each CTA publishes its partial (max, normaliser) per row and bumps the job's
+//   arrival counter; every CTA's pass-2 warps wait (bounded) for the count to reach g
+//   and merge the g partials themselves, eight loads in flight per row.
 // * Pass 2, per key tile: S^T = K . Q^T (M = 128 keys, N = rows rounded up to 16);
 //   the pass-2 warps (one thread per key and row half) sum exp2(s*c - (m + log2 z))
 //   over their rows in registers -- no cross-lane reduction -- and write the vote.
@@ -63,7 +65,6 @@ constexpr int C_XFULL = 160;    // 2 (local statistics hand-off, g == 1)
 constexpr int C_XEMPTY = 176;   // 2
 constexpr int C_TMEM = 192;
 constexpr int C_ABORT = 196;
-constexpr int C_LAST = 200;
 constexpr int C_XSTAT = 256;    // float2 [2][128]  (2048 B)
 constexpr int C_OFF = 2304;     // float [128]
 constexpr int C_ROWPOS = 2816;  // int [128]
@@ -77,9 +78,7 @@ struct WVP {
   float *votes;          // [units, L]
   int atomic_votes;      // several row tiles add into the same votes
   float2 *part;          // [jobs][g][128] per-CTA row statistics (g > 1)
-  float2 *fin;           // [jobs][128] combined statistics (g > 1)
   int *arrive;           // [jobs] arrival counters (zeroed before launch)
-  int *ready;            // [jobs] published flags (zeroed before launch)
   uint32_t *status;
   unsigned long long timeout;
 };
@@ -107,6 +106,13 @@ __device__ __forceinline__ Job job_geo(const WVP &p, int j, int xg) {
   return J;
 }
 
+// (M, Z) <- the statistics of the union of two key sets, Z relative to max M (log2 domain)
+__device__ __forceinline__ void merge_stat(float &M, float &Z, float2 o) {
+  const float Mn = fmaxf(M, o.x);
+  if (Mn != -INFINITY) Z = Z * ex2(M - Mn) + o.y * ex2(o.x - Mn);
+  M = Mn;
+}
+
 // Order of the tile events of one round: first LEAD pass-1 tiles of the new job (A),
 // then alternate pass-2 tiles of the previous job (B) and pass-1 tiles.
 __device__ __forceinline__ bool next_is_a(int ia, int ib, int na, int nb) {
@@ -128,7 +134,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t *ctrl = smem + G::OFF_CTRL;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctrl + C_TMEM);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl + C_ABORT);
-  volatile int *last_flag = reinterpret_cast<volatile int *>(ctrl + C_LAST);
   float2 *xstat = reinterpret_cast<float2 *>(ctrl + C_XSTAT);
   float *off = reinterpret_cast<float *>(ctrl + C_OFF);
   int *rowpos = reinterpret_cast<int *>(ctrl + C_ROWPOS);
@@ -354,25 +359,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (lane == 0) mbar_arrive(ctl + C_XFULL + 8 * xb);
           }
         } else {
+          // publish this CTA's partial statistics; the consumers combine all g of them
           p.part[((size_t)j * p.g + xg) * TILE + lrow] = make_float2(m, z);
           __threadfence();
           named_bar(4, 128);
-          if (lrow == 0) *last_flag = (atomicAdd(&p.arrive[j], 1) == p.g - 1);
-          named_bar(4, 128);
-          if (*last_flag) {
-            __threadfence();
-            float M = -INFINITY, Z = 0.f;
-            for (int r = 0; r < p.g; ++r) {
-              const float2 o2 = __ldcg(p.part + ((size_t)j * p.g + r) * TILE + lrow);
-              const float Mn = fmaxf(M, o2.x);
-              if (Mn != -INFINITY) Z = Z * ex2(M - Mn) + o2.y * ex2(o2.x - Mn);
-              M = Mn;
-            }
-            p.fin[(size_t)j * TILE + lrow] = make_float2(M, Z);
-            __threadfence();
-            named_bar(4, 128);
-            if (lrow == 0) atomicExch(&p.ready[j], 1);
-          }
+          if (lrow == 0) atomicAdd(&p.arrive[j], 1);
         }
       }
     }
@@ -409,7 +400,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       } else {
         if (t2 == 0) {
           bool fine = ok && !ab.raised();
-          if (fine && !spin_flag_bounded(&p.ready[j], p.status, p.timeout)) {
+          if (fine && !spin_count_bounded(&p.arrive[j], p.g, p.status, p.timeout)) {
             ab.raise();
             fine = false;
           }
@@ -417,10 +408,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         named_bar(3, 256);
         ok = ok && (*go != 0);
-        if (t2 < TILE) {
-          const float2 o = __ldcg(p.fin + (size_t)j * TILE + t2);
-          M = o.x;
-          Z = o.y;
+        if (t2 < TILE && ok) {
+          // combine the g partials of this row (in CTA order), eight loads in flight
+          const float2 *src = p.part + (size_t)j * p.g * TILE + t2;
+          M = -INFINITY;
+          int r = 0;
+          for (; r + 8 <= p.g; r += 8) {
+            float2 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __ldcg(src + (size_t)(r + i) * TILE);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) merge_stat(M, Z, v[i]);
+          }
+          for (; r < p.g; ++r) merge_stat(M, Z, __ldcg(src + (size_t)r * TILE));
         }
       }
       if (t2 < TILE) {
@@ -538,8 +538,7 @@ WindowVotePlan plan_window_vote(int units, int L, int R, int Wq, int num_sms) {
   size_t b = 0;
   if (pl.g > 1) {
     b += (size_t)pl.jobs * pl.g * TILE * sizeof(float2);  // part
-    b += (size_t)pl.jobs * TILE * sizeof(float2);         // fin
-    b += 2 * (size_t)pl.jobs * sizeof(int);               // arrive, ready
+    b += (size_t)pl.jobs * sizeof(int);                   // arrive
   }
   pl.ws_bytes = (b + 255) & ~(size_t)255;
   return pl;
@@ -580,15 +579,13 @@ cudaError_t launch_window_vote(const Ctx &c, const WindowVoteArgs &a) {
   uint8_t *w = reinterpret_cast<uint8_t *>(a.ws);
   const size_t jobs = (size_t)p.jobs;
   p.part = reinterpret_cast<float2 *>(w);
-  p.fin = p.part + jobs * p.g * TILE;
-  p.arrive = reinterpret_cast<int *>(p.fin + jobs * TILE);
-  p.ready = p.arrive + jobs;
+  p.arrive = reinterpret_cast<int *>(p.part + jobs * p.g * TILE);
   p.status = c.status;
   p.timeout = c.timeout_ns;
   const int P = c.num_sms;  // one persistent CTA per SM
 
   if (p.g > 1) {
-    e = cudaMemsetAsync(p.arrive, 0, 2 * jobs * sizeof(int), c.stream);
+    e = cudaMemsetAsync(p.arrive, 0, jobs * sizeof(int), c.stream);
     if (e != cudaSuccess) return e;
   }
   if (p.atomic_votes) {
