@@ -77,22 +77,6 @@ struct DecP {
   unsigned long long timeout;
 };
 
-// packed fp32x2 helpers: a 64-bit register holds two fp32 lanes
-__device__ __forceinline__ unsigned long long pk(float lo, float hi) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ float2 upk(unsigned long long v) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-  return r;
-}
-// d += a * b, lane-wise on two fp32 values
-__device__ __forceinline__ void ffma2(unsigned long long &d, unsigned long long a,
-                                      unsigned long long b) {
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
-}
 // the two bf16 of a packed word as a fp32x2 pair
 __device__ __forceinline__ unsigned long long bf2(uint32_t w) {
   return pk(bf_lo(w), bf_hi(w));

@@ -14,7 +14,7 @@
 // * Row statistics are combined across the g CTAs of the job through global memory:
 //   each CTA publishes its partial (max, normaliser) per row and bumps the job's
 //   arrival counter; every CTA's pass-2 warps wait (bounded) for the count to reach g
-//   and merge the g partials themselves, eight loads in flight per row.
+//   and merge the g partials themselves (20 loads in flight per row).
 // * Pass 2, per key tile: S^T = K . Q^T (M = 128 keys, N = rows rounded up to 16);
 //   the pass-2 warps (one thread per key and row half) sum exp2(s*c - (m + log2 z))
 //   over their rows in registers -- no cross-lane reduction -- and write the vote.
@@ -22,7 +22,9 @@
 //   tiles), so the re-read of job k's keys comes from L2 and the statistics exchange
 //   is hidden behind useful work.
 // * Warp roles: warp 0 = TMA producer (Q tiles double-buffered, K tiles in a 4-stage
-//   ring, 128-byte swizzle), warp 1 = TMEM owner and MMA issuer, warps 2-9 = pass 1
+//   ring, 128-byte swizzle), warp 1 = TMEM owner and pass-1 MMA issuer, warp 18 =
+//   pass-2 MMA issuer (separate issuers: tcgen05.mma issue is paced by the tensor pipe,
+//   and a pass-2 tile waiting for statistics must not stall pass 1), warps 2-9 = pass 1
 //   (two warps per TMEM lane quarter, each on half of the tile's key columns), warps
 //   10-17 = pass 2 (two per lane quarter, each on half of the query rows; the halves
 //   of a key's vote meet in shared memory).  Every wait is bounded (KVC_DEV_TIMEOUT).
@@ -35,9 +37,11 @@ namespace {
 
 constexpr int TILE = 128;       // keys per tile; query rows per job
 constexpr int NSTAGE = 4;       // K tile ring depth
-constexpr int NTHREADS = 576;   // 18 warps: TMA, MMA, 8 pass-1 and 8 pass-2 warps
+constexpr int NWARPS = 19;      // TMA, pass-1 MMA, 8 pass-1 warps, 8 pass-2 warps, pass-2 MMA
+constexpr int NTHREADS = 32 * NWARPS;
 constexpr int TMEM_COLS = 512;  // 4 accumulators of 128 fp32 columns
 constexpr int LEAD = 2;         // pass-1 tiles of job k+1 issued before pass 2 of job k
+constexpr int XB = 20;          // partial statistics loaded per batch (group sizes up to 20: one)
 
 template <int D>
 struct Geo {
@@ -66,11 +70,12 @@ constexpr int C_XEMPTY = 176;   // 2
 constexpr int C_TMEM = 192;
 constexpr int C_ABORT = 196;
 constexpr int C_XSTAT = 256;    // float2 [2][128]  (2048 B)
-constexpr int C_OFF = 2304;     // float [128]
+constexpr int C_OFF = 2304;     // float [128] (16-byte aligned: read as float4)
 constexpr int C_ROWPOS = 2816;  // int [128]
 constexpr int C_GO = 3328;      // int: pass-2 warps may proceed (g > 1)
 constexpr int C_HSTAT = 3456;   // float2 [2][128]: second column half's row statistics
 constexpr int C_VPART = 5504;   // float [2][128]: second row half's partial votes
+constexpr int C_TAG = 6528;     // int [NSTAGE]: index of the tile most recently loaded into each stage
 
 struct WVP {
   int L, R, Wq, row_tiles, jobs, g, ngroups;
@@ -106,11 +111,56 @@ __device__ __forceinline__ Job job_geo(const WVP &p, int j, int xg) {
   return J;
 }
 
+// Bounded wait until the producer has tagged a ring stage with tile `want`.
+__device__ __forceinline__ bool wait_tag(volatile int *tag, int want, const Abort &ab) {
+  if (*tag == want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 26); ++it) {
+    if (*tag == want) return true;
+    if (ab.raised()) return false;
+    if ((it & 15u) == 0 && globaltimer_ns() - t0 > ab.limit) break;
+    __nanosleep(32);
+  }
+  ab.raise();
+  return false;
+}
+
 // (M, Z) <- the statistics of the union of two key sets, Z relative to max M (log2 domain)
 __device__ __forceinline__ void merge_stat(float &M, float &Z, float2 o) {
   const float Mn = fmaxf(M, o.x);
   if (Mn != -INFINITY) Z = Z * ex2(M - Mn) + o.y * ex2(o.x - Mn);
   M = Mn;
+}
+
+// Pass-2 sums over w (<= W) rows of one key: exp2(s * c + noff) in packed fp32x2 pairs
+// (noff = -(row max + log2 normaliser), -inf for padding rows).  noff is 16-byte aligned.
+template <int W>
+__device__ __forceinline__ void vote_full(const float *s, const float *noff, unsigned long long cc,
+                                          int w, unsigned long long &a0, unsigned long long &a1) {
+#pragma unroll
+  for (int c = 0; c < W; c += 4) {
+    if (c < w) {
+      const float4 o = *reinterpret_cast<const float4 *>(noff + c);
+      const float2 x = upk(fma2(pk(s[c], s[c + 1]), cc, pk(o.x, o.y)));
+      const float2 y = upk(fma2(pk(s[c + 2], s[c + 3]), cc, pk(o.z, o.w)));
+      a0 = add2(a0, pk(ex2(x.x), ex2(x.y)));
+      a1 = add2(a1, pk(ex2(y.x), ex2(y.y)));
+    }
+  }
+}
+// The same for a key on the causal diagonal: rows whose position precedes the key add 0.
+template <int W>
+__device__ __forceinline__ float vote_masked(const float *s, const float *noff, const int *rowpos,
+                                             float c, int key, int w) {
+  float v = 0.f;
+#pragma unroll
+  for (int i = 0; i < W; ++i) {
+    if (i < w) {
+      const float e = ex2(fmaf(s[i], c, noff[i]));
+      v += (key <= rowpos[i]) ? e : 0.f;
+    }
+  }
+  return v;
 }
 
 // Order of the tile events of one round: first LEAD pass-1 tiles of the new job (A),
@@ -135,7 +185,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ctrl + C_TMEM);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl + C_ABORT);
   float2 *xstat = reinterpret_cast<float2 *>(ctrl + C_XSTAT);
-  float *off = reinterpret_cast<float *>(ctrl + C_OFF);
+  float *noff = reinterpret_cast<float *>(ctrl + C_OFF);  // -(row max + log2 normaliser)
   int *rowpos = reinterpret_cast<int *>(ctrl + C_ROWPOS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -145,13 +195,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     *abort_flag = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(ctl + C_QFULL + 8 * i, 1);
-      mbar_init(ctl + C_QEMPTY + 8 * i, 1);
+      mbar_init(ctl + C_QEMPTY + 8 * i, 2);  // both passes release the Q tile
       mbar_init(ctl + C_XFULL + 8 * i, 4);
       mbar_init(ctl + C_XEMPTY + 8 * i, 4);
     }
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(ctl + C_KFULL + 8 * s, 1);
       mbar_init(ctl + C_KEMPTY + 8 * s, 1);
+      reinterpret_cast<volatile int *>(ctrl + C_TAG)[s] = -1;
     }
     for (int b = 0; b < 4; ++b) {
       mbar_init(ctl + C_SFULL + 8 * b, 1);
@@ -175,6 +226,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int gamma = blockIdx.x / p.g, xg = blockIdx.x - gamma * p.g;
   const int njobs = gamma < p.jobs ? (p.jobs - gamma + p.ngroups - 1) / p.ngroups : 0;
 
+  volatile int *tag = reinterpret_cast<volatile int *>(ctrl + C_TAG);
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
@@ -209,6 +261,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           const int s = kit % NSTAGE, use = kit / NSTAGE;
           if (!ab.wait(ctl + C_KEMPTY + 8 * s, (use & 1) ^ 1)) { ok = false; break; }
+          tag[s] = kit;  // this stage's phase now belongs to tile kit
           mbar_arrive_expect_tx(ctl + C_KFULL + 8 * s, G::TILE_BYTES);
           for (int kb = 0; kb < G::KB; ++kb)
             tma_load_2d(sK + s * G::TILE_BYTES + kb * G::KBLK, &tk, kb * 64, row,
@@ -225,12 +278,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int qb = 0; qb < 2; ++qb)
         if (qcnt[qb] > 0) mbar_wait_bounded(ctl + C_QFULL + 8 * qb, (qcnt[qb] - 1) & 1, p.timeout);
     }
-  } else if (warp == 1) {
-    // -------------------------------- MMA issuer -------------------------------
+  } else if (warp == 1 || warp == NWARPS - 1) {
+    // ---------- MMA issuers: warp 1 for pass-1 tiles, the last warp for pass-2 tiles ----------
+    // Both walk the producer's tile order (which gives each tile's ring stage) and issue
+    // only their own pass's tiles, so a pass-2 tile held up by the statistics exchange
+    // never holds up pass 1.
     if (lane == 0) {
-      int kit = 0, it1 = 0, it2 = 0, last_bar = -1, last_par = 0, qcnt[2] = {0, 0};
+      const bool mine_a = warp == 1;
+      int kit = 0, it = 0, last_bar = -1, last_par = 0, qcnt[2] = {0, 0};
       bool ok = true;
-      const uint32_t idesc1 = idesc_bf16(128, TILE);
       Job Jb{};
       for (int k = 0; k <= njobs && ok; ++k) {
         Job Ja{};
@@ -240,44 +296,50 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           na = Ja.t1 - Ja.t0;
         }
         if (k >= 1) nb = Jb.t1 - Jb.t0;
-        if (na > 0) {
-          if (!ab.wait(ctl + C_QFULL + 8 * (k & 1), qcnt[k & 1] & 1)) { ok = false; break; }
-          ++qcnt[k & 1];
+        // this issuer's job of the round (pass 1: job k, pass 2: job k-1) and its Q buffer
+        const int nmine = mine_a ? na : nb;
+        const int qb = (mine_a ? k : k - 1) & 1;
+        if (nmine > 0) {
+          if (!ab.wait(ctl + C_QFULL + 8 * qb, qcnt[qb] & 1)) { ok = false; break; }
+          ++qcnt[qb];
           tc_fence_after();
         }
-        const uint32_t idesc2 = idesc_bf16(128, Jb.rpad > 0 ? Jb.rpad : 16);
+        const uint32_t idesc = idesc_bf16(128, mine_a ? TILE : (Jb.rpad > 0 ? Jb.rpad : 16));
+        const uint64_t qd = sdesc_k128(sQ + qb * G::TILE_BYTES);
         for (int ia = 0, ib = 0; ia < na || ib < nb;) {
           const bool isa = next_is_a(ia, ib, na, nb);
-          int b, use;
-          if (isa) { b = it1 & 1; use = it1 >> 1; }
-          else { b = 2 + (it2 & 1); use = it2 >> 1; }
+          if (isa) ++ia; else ++ib;
           const int s = kit % NSTAGE, kuse = kit / NSTAGE;
+          ++kit;
+          if (isa != mine_a) continue;
+          const int b = (mine_a ? 0 : 2) + (it & 1), use = it >> 1;
+          ++it;
+          // An issuer may run a whole round ahead of the producer; the stage's parity only
+          // identifies the tile once the producer has started loading it.
+          if (!wait_tag(tag + s, kit - 1, ab)) { ok = false; break; }
           if (!ab.wait(ctl + C_KFULL + 8 * s, kuse & 1)) { ok = false; break; }
           if (!ab.wait(ctl + C_SEMPTY + 8 * b, (use & 1) ^ 1)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d = tmem + (uint32_t)(b * 128);
-          const uint32_t qa = sQ + (isa ? (k & 1) : ((k - 1) & 1)) * G::TILE_BYTES;
-          const uint32_t ka = sK + s * G::TILE_BYTES;
+          // descriptors of the tile's first 16-wide k-step; later k-steps advance the
+          // start address field (bytes / 16) by a constant
+          const uint64_t kd = sdesc_k128(sK + s * G::TILE_BYTES);
+          const uint64_t ad = mine_a ? qd : kd, bd = mine_a ? kd : qd;
 #pragma unroll
           for (int kb = 0; kb < G::KB; ++kb) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint32_t o = kb * G::KBLK + kk * 32;
-              if (isa)
-                umma_bf16(d, sdesc_k128(qa + o), sdesc_k128(ka + o), idesc1, (kb | kk) != 0);
-              else
-                umma_bf16(d, sdesc_k128(ka + o), sdesc_k128(qa + o), idesc2, (kb | kk) != 0);
+              const uint64_t o = (uint64_t)((kb * G::KBLK + kk * 32) >> 4);
+              umma_bf16(d, ad + o, bd + o, idesc, (kb | kk) != 0);
             }
           }
           umma_commit(ctl + C_KEMPTY + 8 * s);
           umma_commit(ctl + C_SFULL + 8 * b);
           last_bar = b;
           last_par = use & 1;
-          ++kit;
-          if (isa) { ++ia; ++it1; } else { ++ib; ++it2; }
         }
         if (!ok) break;
-        if (nb > 0) umma_commit(ctl + C_QEMPTY + 8 * ((k - 1) & 1));  // job k-1 done with Q
+        if (nmine > 0) umma_commit(ctl + C_QEMPTY + 8 * qb);  // this pass is done with the Q tile
         Jb = Ja;
       }
       // drain: wait for the completion of the last MMA batch issued
@@ -327,13 +389,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           const float mnew = fmaxf(m, fmaxf(mx0, mx1) * p.c);
           if (mnew != -INFINITY) {
-            float acc0 = 0.f, acc1 = 0.f;
+            // exp2(s * c - m) summed in packed fp32x2 pairs
+            const unsigned long long cc = pk(p.c, p.c), nm = pk(-mnew, -mnew);
+            unsigned long long a0 = 0ull, a1 = 0ull;
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-              acc0 += ex2(fmaf(s[c], p.c, -mnew));
-              acc1 += ex2(fmaf(s[c + 1], p.c, -mnew));
+            for (int c = 0; c < 64; c += 4) {
+              const float2 x = upk(fma2(pk(s[c], s[c + 1]), cc, nm));
+              const float2 y = upk(fma2(pk(s[c + 2], s[c + 3]), cc, nm));
+              a0 = add2(a0, pk(ex2(x.x), ex2(x.y)));
+              a1 = add2(a1, pk(ex2(y.x), ex2(y.y)));
             }
-            z = z * ex2(m - mnew) + (acc0 + acc1);
+            const float2 a = upk(add2(a0, a1));
+            z = z * ex2(m - mnew) + (a.x + a.y);
             m = mnew;
           }
         }
@@ -409,75 +476,63 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         named_bar(3, 256);
         ok = ok && (*go != 0);
         if (t2 < TILE && ok) {
-          // combine the g partials of this row (in CTA order), eight loads in flight
+          // combine the g partials of this row (in CTA order), up to XB loads in flight
           const float2 *src = p.part + (size_t)j * p.g * TILE + t2;
           M = -INFINITY;
-          int r = 0;
-          for (; r + 8 <= p.g; r += 8) {
-            float2 v[8];
+          for (int r = 0; r < p.g; r += XB) {
+            float2 v[XB];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __ldcg(src + (size_t)(r + i) * TILE);
+            for (int i = 0; i < XB; ++i)
+              v[i] = r + i < p.g ? __ldcg(src + (size_t)(r + i) * TILE) : make_float2(-INFINITY, 0.f);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) merge_stat(M, Z, v[i]);
+            for (int i = 0; i < XB; ++i) merge_stat(M, Z, v[i]);
           }
-          for (; r < p.g; ++r) merge_stat(M, Z, __ldcg(src + (size_t)r * TILE));
         }
       }
       if (t2 < TILE) {
         const bool rvalid = t2 < J.nrows;
-        off[t2] = (rvalid && Z > 0.f) ? M + lg2(Z) : INFINITY;
+        noff[t2] = (rvalid && Z > 0.f) ? -(M + lg2(Z)) : -INFINITY;
         rowpos[t2] = rvalid ? p.L - p.Wq + (J.rho0 + t2) % p.Wq : -1;
       }
       named_bar(3, 256);
       const int half = J.rpad >> 1;  // rows per half: a multiple of 8
       const int r_lo = rh * half;
+      const unsigned long long cc = pk(p.c, p.c);
       for (int i = 0; i < n; ++i, ++it2) {
         const int b = 2 + (it2 & 1);
         const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_SFULL + 8 * b, (it2 >> 1) & 1));
         ok = got;
         const int key = (J.t1 - 1 - i) * TILE + lkey;
-        float v0 = 0.f, v1 = 0.f;
+        float v0 = 0.f;
         if (got) {
           tc_fence_after();
           const bool kfull = key <= J.pmin;
+          unsigned long long a0 = 0ull, a1 = 0ull;
+          const uint32_t ta = tmem + lane_base + (uint32_t)(b * 128 + r_lo);
           for (int c0 = 0; c0 < half;) {
             const int w = half - c0 >= 32 ? 32 : (half - c0 >= 16 ? 16 : 8);
             const int r0 = r_lo + c0;
-            const uint32_t ta = tmem + lane_base + (uint32_t)(b * 128 + r0);
             float s[32];
-            if (w == 32) tmem_ld32(ta, s);
-            else if (w == 16) tmem_ld16(ta, s);
-            else tmem_ld8(ta, s);
+            if (w == 32) tmem_ld32(ta + c0, s);
+            else if (w == 16) tmem_ld16(ta + c0, s);
+            else tmem_ld8(ta + c0, s);
             tmem_wait_ld();
-            if (kfull) {
-#pragma unroll
-              for (int c = 0; c < 32; c += 2) {
-                if (c < w) {
-                  v0 += ex2(fmaf(s[c], p.c, -off[r0 + c]));
-                  v1 += ex2(fmaf(s[c + 1], p.c, -off[r0 + c + 1]));
-                }
-              }
-            } else {
-#pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                if (c < w) {
-                  const float e = ex2(fmaf(s[c], p.c, -off[r0 + c]));
-                  v0 += (key <= rowpos[r0 + c]) ? e : 0.f;
-                }
-              }
-            }
+            if (kfull) vote_full<32>(s, noff + r0, cc, w, a0, a1);
+            else v0 += vote_masked<32>(s, noff + r0, rowpos + r0, p.c, key, w);
             c0 += w;
           }
+          const float2 a = upk(add2(a0, a1));
+          v0 += a.x + a.y;
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(ctl + C_SEMPTY + 8 * b);
         }
         // the two row halves of this key meet in shared memory (one pair barrier per tile)
         const int par = it2 & 1;
-        if (rh == 1) vpart[par * TILE + lkey] = v0 + v1;
+        if (rh == 1) vpart[par * TILE + lkey] = v0;
         named_bar(8 + quarter, 64);
         if (rh == 0 && got && key < J.kend) {
-          const float v = v0 + v1 + vpart[par * TILE + lkey];
+          const float v = v0 + vpart[par * TILE + lkey];
           float *dst = p.votes + (size_t)J.u * p.L + key;
           if (p.atomic_votes)
             atomicAdd(dst, v);

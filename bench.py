@@ -319,6 +319,8 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     status |= kvc.kvc_device_status()
+    if status:  # a kernel gave up on a bounded wait: its results and timings are invalid
+        raise RuntimeError("device status flags %#x after the timed steps" % status)
     total_ms = t_all0.elapsed_time(t_all1)
     comp_ms = [a.elapsed_time(b) for a, b, c in recs]
     comp_avg = sum(comp_ms) / len(comp_ms)
@@ -379,6 +381,9 @@ def run_ours(args):
         for _ in range(max(1, min(args.steps, 3))):
             e2e_step(erec)
         torch.cuda.synchronize()
+        e2e_status = kvc.kvc_device_status()
+        if e2e_status:
+            raise RuntimeError("device status flags %#x after the end-to-end steps" % e2e_status)
         comp_e2e = statistics.median(a.elapsed_time(b) for a, b, c in erec)
         all_e2e = statistics.median(a.elapsed_time(c) for a, b, c in erec)
         e2e = {"value": ws * B * L / (comp_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
