@@ -132,21 +132,60 @@ __device__ __forceinline__ void merge_stat(float &M, float &Z, float2 o) {
   M = Mn;
 }
 
-// Pass-2 sums over w (<= W) rows of one key: exp2(s * c + noff) in packed fp32x2 pairs
-// (noff = -(row max + log2 normaliser), -inf for padding rows).  noff is 16-byte aligned.
-template <int W>
-__device__ __forceinline__ void vote_full(const float *s, const float *noff, unsigned long long cc,
-                                          int w, unsigned long long &a0, unsigned long long &a1) {
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of 64 values: eight independent chains of three-input max, then a short tree
+// (a single chain would expose the max latency 32 times).
+__device__ __forceinline__ float max64(const float *s) {
+  float m[8];
 #pragma unroll
-  for (int c = 0; c < W; c += 4) {
-    if (c < w) {
-      const float4 o = *reinterpret_cast<const float4 *>(noff + c);
-      const float2 x = upk(fma2(pk(s[c], s[c + 1]), cc, pk(o.x, o.y)));
-      const float2 y = upk(fma2(pk(s[c + 2], s[c + 3]), cc, pk(o.z, o.w)));
-      a0 = add2(a0, pk(ex2(x.x), ex2(x.y)));
-      a1 = add2(a1, pk(ex2(y.x), ex2(y.y)));
-    }
+  for (int j = 0; j < 8; ++j) m[j] = fmax3(s[j], s[j + 8], s[j + 16]);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m[j] = fmax3(m[j], s[j + 24], s[j + 32]);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m[j] = fmax3(m[j], s[j + 40], s[j + 48]);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m[j] = fmaxf(m[j], s[j + 56]);
+  return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
+// Adds exp2(s[i] * c + off[i]) for i < N (N a multiple of 8) into four packed fp32x2
+// accumulators (independent chains).  off is 16-byte aligned.
+template <int N>
+__device__ __forceinline__ void exp2_sum(const float *s, const float *off, unsigned long long cc,
+                                         unsigned long long (&a)[4]) {
+#pragma unroll
+  for (int c = 0; c < N; c += 8) {
+    const float4 o0 = *reinterpret_cast<const float4 *>(off + c);
+    const float4 o1 = *reinterpret_cast<const float4 *>(off + c + 4);
+    const float2 x0 = upk(fma2(pk(s[c], s[c + 1]), cc, pk(o0.x, o0.y)));
+    const float2 x1 = upk(fma2(pk(s[c + 2], s[c + 3]), cc, pk(o0.z, o0.w)));
+    const float2 x2 = upk(fma2(pk(s[c + 4], s[c + 5]), cc, pk(o1.x, o1.y)));
+    const float2 x3 = upk(fma2(pk(s[c + 6], s[c + 7]), cc, pk(o1.z, o1.w)));
+    a[0] = add2(a[0], pk(ex2(x0.x), ex2(x0.y)));
+    a[1] = add2(a[1], pk(ex2(x1.x), ex2(x1.y)));
+    a[2] = add2(a[2], pk(ex2(x2.x), ex2(x2.y)));
+    a[3] = add2(a[3], pk(ex2(x3.x), ex2(x3.y)));
   }
+}
+
+// The sum of the four packed accumulators.
+__device__ __forceinline__ float sum4(const unsigned long long (&a)[4]) {
+  const float2 t = upk(add2(add2(a[0], a[1]), add2(a[2], a[3])));
+  return t.x + t.y;
+}
+
+// Pass 2 over w rows (w = 32, 16 or 8) of one key off the causal diagonal:
+// exp2(s * c + noff) with noff = -(row max + log2 normaliser), -inf for padding rows.
+__device__ __forceinline__ void vote_full(const float *s, const float *noff, unsigned long long cc,
+                                          int w, unsigned long long (&a)[4]) {
+  if (w == 32) exp2_sum<32>(s, noff, cc, a);
+  else if (w == 16) exp2_sum<16>(s, noff, cc, a);
+  else exp2_sum<8>(s, noff, cc, a);
 }
 // The same for a key on the causal diagonal: rows whose position precedes the key add 0.
 template <int W>
@@ -381,26 +420,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int c = 0; c < 64; ++c)
               if (kbase + c > prow) s[c] = -INFINITY;
           }
-          float mx0 = s[0], mx1 = s[1];
-#pragma unroll
-          for (int c = 2; c < 64; c += 2) {
-            mx0 = fmaxf(mx0, s[c]);
-            mx1 = fmaxf(mx1, s[c + 1]);
-          }
-          const float mnew = fmaxf(m, fmaxf(mx0, mx1) * p.c);
+          const float mnew = fmaxf(m, max64(s) * p.c);
           if (mnew != -INFINITY) {
-            // exp2(s * c - m) summed in packed fp32x2 pairs
+            // exp2(s * c - m) summed in packed fp32x2 pairs, four independent chains
             const unsigned long long cc = pk(p.c, p.c), nm = pk(-mnew, -mnew);
-            unsigned long long a0 = 0ull, a1 = 0ull;
+            unsigned long long a[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-              const float2 x = upk(fma2(pk(s[c], s[c + 1]), cc, nm));
-              const float2 y = upk(fma2(pk(s[c + 2], s[c + 3]), cc, nm));
-              a0 = add2(a0, pk(ex2(x.x), ex2(x.y)));
-              a1 = add2(a1, pk(ex2(y.x), ex2(y.y)));
+            for (int c = 0; c < 64; c += 8) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float2 x = upk(fma2(pk(s[c + 2 * q], s[c + 2 * q + 1]), cc, nm));
+                a[q] = add2(a[q], pk(ex2(x.x), ex2(x.y)));
+              }
             }
-            const float2 a = upk(add2(a0, a1));
-            z = z * ex2(m - mnew) + (a.x + a.y);
+            z = z * ex2(m - mnew) + sum4(a);
             m = mnew;
           }
         }
@@ -507,7 +540,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (got) {
           tc_fence_after();
           const bool kfull = key <= J.pmin;
-          unsigned long long a0 = 0ull, a1 = 0ull;
+          unsigned long long a[4] = {0ull, 0ull, 0ull, 0ull};
           const uint32_t ta = tmem + lane_base + (uint32_t)(b * 128 + r_lo);
           for (int c0 = 0; c0 < half;) {
             const int w = half - c0 >= 32 ? 32 : (half - c0 >= 16 ? 16 : 8);
@@ -517,12 +550,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             else if (w == 16) tmem_ld16(ta + c0, s);
             else tmem_ld8(ta + c0, s);
             tmem_wait_ld();
-            if (kfull) vote_full<32>(s, noff + r0, cc, w, a0, a1);
+            if (kfull) vote_full(s, noff + r0, cc, w, a);
             else v0 += vote_masked<32>(s, noff + r0, rowpos + r0, p.c, key, w);
             c0 += w;
           }
-          const float2 a = upk(add2(a0, a1));
-          v0 += a.x + a.y;
+          v0 += sum4(a);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(ctl + C_SEMPTY + 8 * b);
