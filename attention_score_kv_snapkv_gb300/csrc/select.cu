@@ -3,24 +3,37 @@
 // first), then the gather of the kept prefix rows and the kept window into the compact
 // cache.  The same code cuts H2O's prompt to heavy hitters + recent window (pool 1).
 //
-// pool_topk_kernel: one CTA (1024 threads) per unit.
+// pool_topk_kernel: one CTA (512 threads, two per SM) per unit.
 //   phase 0  pooled vote u_j = max(v[j-h .. j+h]) (cut at the candidate range) turned
 //            into an order-preserving uint32 key, kept in shared memory (global
-//            workspace when the candidate range does not fit);
-//   phase 1  radix select of the k-th largest key: three histogram passes over the
-//            11 + 11 + 10 key bits, each narrowing the bucket that holds it;
+//            workspace when the candidate range does not fit); the votes are staged
+//            through shared memory in chunks;
+//   phase 1  radix select of the k-th largest key: four histogram passes over 8-bit
+//            digits, each narrowing the bucket that holds it; every warp counts into
+//            its own histogram, so the few hot bins of the top digit are not contended
+//            across warps;
 //   phase 2  stream compaction in position order: keys above the threshold, and the
 //            first `need` keys equal to it (exact lower-position tie rule), written as
-//            ascending positions.
+//            ascending positions (per-thread runs, one block-wide scan).
 // gather_kernel: 16-byte vectorised copy of the kept K/V rows, positions, scores.
 #include "kvc_internal.cuh"
 
 namespace kvc {
 namespace {
 
-constexpr int NT = 1024;        // threads of pool_topk_kernel
+constexpr int NT = 512;          // threads of pool_topk_kernel (two CTAs per SM)
 constexpr int NWARP = NT / 32;
-constexpr int SMEM_KEYS_MAX = 50 * 1024;  // candidates kept in shared memory
+constexpr int NBIN = 256;        // radix digit of 8 bits, four passes
+constexpr int CHUNK = 4096;      // pooling staging floats (aliases the histograms)
+constexpr int SMEM_KEYS_MAX = 48 * 1024;  // candidates kept in shared memory
+
+constexpr int RUN = 32;          // positions per thread in the kernel-7 pooling path
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   const uint32_t b = __float_as_uint(x);
@@ -35,24 +48,105 @@ struct TopkP {
   uint32_t *kglobal;   // [U, n_cand] keys when they do not fit in shared memory
 };
 
-__global__ void __launch_bounds__(NT, 1) pool_topk_kernel(const TopkP p) {
+// shared memory (32-bit words): per-warp histograms [NWARP][NBIN] (the pooling stage
+// buffer while pooling), merged histogram [NBIN], misc [128], then the keys
+constexpr int SM_HIST = 0;
+constexpr int SM_TOT = NWARP * NBIN;
+constexpr int SM_MISC = SM_TOT + NBIN;
+constexpr int SM_KEYS = SM_MISC + 128;
+static_assert(NWARP * NBIN >= CHUNK, "the pooling stage aliases the histograms");
+// Keys are stored with one pad word per 32 (key j at kidx(j)): a warp reading 32
+// consecutive keys and a thread writing its run of 32 are both free of bank conflicts.
+__host__ __device__ constexpr int kidx(int j) { return j + (j >> 5); }
+// words of the key region: the padded keys, or the padded staging of the votes with a
+// halo of 3 on both sides
+__host__ __device__ constexpr int key_words(int n) { return n + 6 + (n + 6) / 32 + 1; }
+
+__global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
   extern __shared__ uint32_t sm[];
-  uint32_t *hist = sm;                 // 2048 bins
-  int *misc = reinterpret_cast<int *>(sm + 2048);   // [0] prefix, [1] need, [2..33] warp eq, [34..65] warp take
-  uint32_t *keys = sm + 2048 + 128;    // n_cand keys (shared path)
+  uint32_t *tot = sm + SM_TOT;
+  int *misc = reinterpret_cast<int *>(sm + SM_MISC);  // [0] prefix, [1] need, [2..] warp eq, [2+NWARP..] warp gt
   const int u = blockIdx.x;
   const int n = p.n_cand;
   const bool in_smem = n <= SMEM_KEYS_MAX;
-  uint32_t *kb = in_smem ? keys : p.kglobal + (size_t)u * n;
+  uint32_t *kb = in_smem ? sm + SM_KEYS : p.kglobal + (size_t)u * key_words(n);
   const float *v = p.votes + (size_t)u * p.L;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = p.half;
 
-  // phase 0: pooled keys
-  for (int j = tid; j < n; j += NT) {
-    const int lo = max(0, j - p.half), hi = min(n - 1, j + p.half);
-    float m = v[lo];
-    for (int t = lo + 1; t <= hi; ++t) m = fmaxf(m, v[t]);
-    kb[j] = order_key(m);
+  // phase 0: pooled keys u_j = max(v[j-h .. j+h]) cut at the candidate range.  The
+  // votes are staged through shared memory (coalesced, read once from L2): all of them
+  // at once into the key array when it is in shared memory (each thread keeps its
+  // pooled values in registers until every window has been read), else in chunks.
+  if (in_smem && n <= RUN * NT && h == 3) {
+    // pool kernel 7, one run of 32 consecutive positions per thread: the votes go to
+    // shared memory with one pad word per 32 (a thread's run is then conflict-free
+    // across the warp); the run and its halo are read into registers and the window
+    // maxima formed there (three-input max), then written back as keys in place.
+    float *vs = reinterpret_cast<float *>(kb);
+    // eight loads in flight per thread before the stores (a plain loop would wait out
+    // the memory latency once per element)
+    for (int j1 = tid; j1 < n + 6; j1 += 8 * NT) {
+      float t8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int q = j1 + e * NT - 3;  // position, halo of 3 on both sides
+        t8[e] = (q >= 0 && q < n) ? __ldg(v + q) : -INFINITY;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int j = j1 + e * NT;
+        if (j < n + 6) vs[j + (j >> 5)] = t8[e];
+      }
+    }
+    __syncthreads();
+    const int j0 = tid * RUN;
+    float w[RUN + 6];
+#pragma unroll
+    for (int i = 0; i < RUN + 6; ++i) {
+      const int jj = j0 + i;  // staged index of position j0 + i - 3
+      w[i] = jj < n + 6 ? vs[jj + (jj >> 5)] : -INFINITY;
+    }
+    float mx[RUN];
+#pragma unroll
+    for (int i = 0; i < RUN; ++i)
+      mx[i] = fmax3(fmax3(w[i], w[i + 1], w[i + 2]), fmax3(w[i + 3], w[i + 4], w[i + 5]), w[i + 6]);
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < RUN; ++i)
+      if (j0 + i < n) kb[kidx(j0 + i)] = order_key(mx[i]);
+  } else if (2 * h < CHUNK / 2) {
+    float *stage = reinterpret_cast<float *>(sm + SM_HIST);
+    const int step = CHUNK - 2 * h;
+    for (int c0 = 0; c0 < n; c0 += step) {
+      const int lo = c0 - h;
+      for (int i1 = tid; i1 < CHUNK; i1 += 8 * NT) {
+        float t8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = lo + i1 + e * NT;
+          t8[e] = (i1 + e * NT < CHUNK && j >= 0 && j < n) ? __ldg(v + j) : -INFINITY;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (i1 + e * NT < CHUNK) stage[i1 + e * NT] = t8[e];
+      }
+      __syncthreads();
+      const int cnt = min(step, n - c0);
+      for (int i = tid; i < cnt; i += NT) {
+        float m = stage[i];
+        for (int t = 1; t <= 2 * h; ++t) m = fmaxf(m, stage[i + t]);
+        kb[kidx(c0 + i)] = order_key(m);
+      }
+      __syncthreads();
+    }
+  } else {  // very wide pooling kernels: direct loads
+    for (int j = tid; j < n; j += NT) {
+      const int lo = max(0, j - h), hi = min(n - 1, j + h);
+      float m = v[lo];
+      for (int t = lo + 1; t <= hi; ++t) m = fmaxf(m, v[t]);
+      kb[kidx(j)] = order_key(m);
+    }
   }
   if (tid == 0) {
     misc[0] = 0;      // prefix of the threshold key
@@ -60,36 +154,52 @@ __global__ void __launch_bounds__(NT, 1) pool_topk_kernel(const TopkP p) {
   }
   __syncthreads();
 
-  // phase 1: radix select of the k-th largest key
+  // phase 1: radix select of the k-th largest key, four 8-bit digits from the top.
+  // Each warp counts into its own histogram (no contention between warps; within a
+  // warp, one shared atomic per distinct bin), then the histograms are merged.
   uint32_t mask_hi = 0;
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
+  uint32_t *whist = sm + SM_HIST + warp * NBIN;
 #pragma unroll 1
-  for (int d = 0; d < 3; ++d) {
-    const int sh = shifts[d], w = widths[d], nb = 1 << w;
-    for (int i = tid; i < nb; i += NT) hist[i] = 0;
-    __syncthreads();
+  for (int d = 0; d < 4; ++d) {
+    const int sh = 24 - 8 * d;
+    for (int b = lane; b < NBIN; b += 32) whist[b] = 0;
+    __syncwarp();
     const uint32_t prefix = (uint32_t)misc[0];
-    // warp-aggregated counting: one shared atomic per distinct bin per warp (the first
-    // digit puts most keys into a handful of bins)
-    for (int j0 = warp * 32; j0 < n; j0 += NT) {
-      const int j = j0 + lane;
-      const uint32_t key = j < n ? kb[j] : 0u;
-      const bool valid = j < n && (key & mask_hi) == prefix;
-      const uint32_t vm = __ballot_sync(0xffffffffu, valid);
-      if (valid) {
-        const uint32_t bin = (key >> sh) & (nb - 1);
-        const uint32_t grp = __match_any_sync(vm, bin);
-        if (lane == __ffs(grp) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(grp));
+    if (d == 0) {
+      // the top digit (sign and high exponent bits) puts most keys into a few bins:
+      // one atomic per distinct bin of the warp
+      for (int j0 = warp * 32; j0 < n; j0 += NT) {
+        const int j = j0 + lane;
+        const uint32_t key = j < n ? kb[kidx(j)] : 0u;
+        const uint32_t vm = __ballot_sync(0xffffffffu, j < n);
+        if (j < n) {
+          const uint32_t bin = key >> sh;
+          const uint32_t grp = __match_any_sync(vm, bin);
+          if (lane == __ffs(grp) - 1) atomicAdd(&whist[bin], (uint32_t)__popc(grp));
+        }
       }
+    } else {
+      // lower digits of the keys left in the bucket: spread bins, plain atomics
+      for (int j = warp * 32 + lane; j < n; j += NT) {
+        const uint32_t key = kb[kidx(j)];
+        if ((key & mask_hi) == prefix) atomicAdd(&whist[(key >> sh) & (NBIN - 1)], 1u);
+      }
+    }
+    __syncthreads();
+    for (int b = tid; b < NBIN; b += NT) {
+      uint32_t s = 0;
+#pragma unroll 4
+      for (int w = 0; w < NWARP; ++w) s += sm[SM_HIST + w * NBIN + b];
+      tot[b] = s;
     }
     __syncthreads();
     if (warp == 0) {
       const int need = misc[1];
-      const int per = nb / 32;
+      constexpr int per = NBIN / 32;
       // lane l owns bins [l*per, (l+1)*per); sum, then suffix sums from the top lane
       uint32_t s = 0;
-      for (int b = 0; b < per; ++b) s += hist[lane * per + b];
+#pragma unroll
+      for (int b = 0; b < per; ++b) s += tot[lane * per + b];
       uint32_t incl = s;  // keys in bins owned by this lane and every higher lane
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -101,58 +211,73 @@ __global__ void __launch_bounds__(NT, 1) pool_topk_kernel(const TopkP p) {
       if (mine) {
         uint32_t acc = above;
         for (int b = per - 1; b >= 0; --b) {
-          const uint32_t h = hist[lane * per + b];
-          if (acc + h >= (uint32_t)need) {
+          const uint32_t hb = tot[lane * per + b];
+          if (acc + hb >= (uint32_t)need) {
             misc[0] = (int)(prefix | ((uint32_t)(lane * per + b) << sh));
             misc[1] = need - (int)acc;
             break;
           }
-          acc += h;
+          acc += hb;
         }
       }
     }
-    mask_hi |= (uint32_t)(nb - 1) << sh;
+    mask_hi |= (uint32_t)(NBIN - 1) << sh;
     __syncthreads();
   }
   const uint32_t T = (uint32_t)misc[0];
   const int need = misc[1];
 
-  // phase 2: compaction in position order; warp w owns positions [w*blk, (w+1)*blk)
-  const int blk = ((n + NWARP - 1) / NWARP + 31) & ~31;
-  const int b0 = warp * blk, b1 = min(n, b0 + blk);
-  int eq_cnt = 0, gt_cnt = 0;
-  for (int j0 = b0; j0 < b1; j0 += 32) {
-    const int j = j0 + lane;
-    const uint32_t key = j < b1 ? kb[j] : 0u;
-    eq_cnt += __popc(__ballot_sync(0xffffffffu, j < b1 && key == T));
-    gt_cnt += __popc(__ballot_sync(0xffffffffu, j < b1 && key > T));
-  }
-  if (lane == 0) {
-    misc[2 + warp] = eq_cnt;
-    misc[34 + warp] = gt_cnt;
-  }
-  __syncthreads();
-  int eq_base = 0, out_base = 0;
-  for (int w2 = 0; w2 < warp; ++w2) {
-    const int e = misc[2 + w2], g = misc[34 + w2];
-    const int take_eq = max(0, min(e, need - eq_base));
-    out_base += g + take_eq;
-    eq_base += e;
-  }
+  // phase 2: compaction in position order.  Positions go in super-chunks of NT * RUN;
+  // within one, thread t owns the run [t*RUN, (t+1)*RUN): it counts its keys above and
+  // equal to the threshold, a block-wide exclusive scan gives its output offset, and it
+  // writes its chosen positions (ties: the first `need` equal keys by position).
   int32_t *sel = p.sel + (size_t)u * p.cap;
-  const uint32_t lt = (1u << lane) - 1u;
-  for (int j0 = b0; j0 < b1; j0 += 32) {
-    const int j = j0 + lane;
-    const uint32_t key = j < b1 ? kb[j] : 0u;
-    const bool eq = j < b1 && key == T, gt = j < b1 && key > T;
-    const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
-    const int rank = eq_base + __popc(eqm & lt);
-    const bool take = gt || (eq && rank < need);
-    const uint32_t tm = __ballot_sync(0xffffffffu, take);
-    const int slot = out_base + __popc(tm & lt);
-    if (take && slot < p.k) sel[slot] = j;
-    eq_base += __popc(eqm);
-    out_base += __popc(tm);
+  int *wsum = misc + 2;  // per-warp totals of the packed counts
+  int gt_base = 0, eq_base = 0;
+  for (int c0 = 0; c0 < n; c0 += NT * RUN) {
+    const int j0 = c0 + tid * RUN;
+    int gt = 0, eq = 0;
+#pragma unroll 8
+    for (int i = 0; i < RUN; ++i) {
+      const int j = j0 + i;
+      const uint32_t key = j < n ? kb[kidx(j)] : 0u;
+      gt += (j < n && key > T) ? 1 : 0;
+      eq += (j < n && key == T) ? 1 : 0;
+    }
+    // exclusive scan of (gt | eq << 16) over the block
+    const int packed = gt | (eq << 16);
+    int incl = packed;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int wbase = 0, total = 0;
+    for (int w2 = 0; w2 < NWARP; ++w2) {
+      const int x = wsum[w2];
+      if (w2 < warp) wbase += x;
+      total += x;
+    }
+    const int excl = wbase + incl - packed;
+    int gt_before = gt_base + (excl & 0xffff), eq_before = eq_base + (excl >> 16);
+    if (gt + eq > 0) {
+      int out = gt_before + min(eq_before, need);
+      for (int i = 0; i < RUN; ++i) {
+        const int j = j0 + i;
+        if (j >= n) break;
+        const uint32_t key = kb[kidx(j)];
+        const bool take = key > T || (key == T && eq_before++ < need);
+        if (take) {
+          if (out < p.k) sel[out] = j;
+          ++out;
+        }
+      }
+    }
+    gt_base += total & 0xffff;
+    eq_base += total >> 16;
+    __syncthreads();  // wsum is rewritten by the next super-chunk
   }
 }
 
@@ -214,7 +339,7 @@ bool g_topk_attr[64];
 size_t select_ws_bytes(int units, int L, int keep_window, int cap) {
   const size_t n = (size_t)(L > keep_window ? L - keep_window : 0);
   size_t b = (size_t)units * cap * sizeof(int32_t);               // selected positions
-  if (n > (size_t)SMEM_KEYS_MAX) b += (size_t)units * n * sizeof(uint32_t);  // keys
+  if (n > (size_t)SMEM_KEYS_MAX) b += (size_t)units * key_words((int)n) * sizeof(uint32_t);  // keys
   return (b + 255) & ~(size_t)255;
 }
 
@@ -225,11 +350,11 @@ cudaError_t launch_select_gather(const Ctx &c, const SelectArgs &a) {
   if (!a.identity && k_pick > 0) {
     int dev = 0;
     cudaGetDevice(&dev);
-    const int smem = (2048 + 128) * 4 + (n_cand <= SMEM_KEYS_MAX ? n_cand * 4 : 0);
+    const int smem = SM_KEYS * 4 + (n_cand <= SMEM_KEYS_MAX ? key_words(n_cand) * 4 : 0);
     if (dev < 64 && !g_topk_attr[dev]) {
       cudaError_t e = cudaFuncSetAttribute(pool_topk_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (2048 + 128 + SMEM_KEYS_MAX) * 4);
+                                           (SM_KEYS + key_words(SMEM_KEYS_MAX)) * 4);
       if (e != cudaSuccess) return e;
       g_topk_attr[dev] = true;
     }
