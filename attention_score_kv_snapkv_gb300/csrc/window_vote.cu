@@ -37,10 +37,14 @@ namespace {
 
 constexpr int TILE = 128;       // keys per tile; query rows per job
 constexpr int NSTAGE = 4;       // K tile ring depth
+constexpr int NQ = 2;           // Q tile buffers (a job's tile stays until its pass 2 is done)
+constexpr int LAG = 1;          // round r streams pass 1 of job r and pass 2 of job r - LAG
+static_assert(NQ >= LAG + 1, "the Q tiles of jobs r - LAG .. r must be resident together");
 constexpr int NWARPS = 19;      // TMA, pass-1 MMA, 8 pass-1 warps, 8 pass-2 warps, pass-2 MMA
 constexpr int NTHREADS = 32 * NWARPS;
 constexpr int TMEM_COLS = 512;  // 4 accumulators of 128 fp32 columns
-constexpr int LEAD = 2;         // pass-1 tiles of job k+1 issued before pass 2 of job k
+constexpr int LEAD = 2;         // pass-1 tiles of a round issued before its first pass-2 tile
+constexpr int PF = 0;           // pass-1 tiles prefetched into L2 ahead of the ring
 constexpr int XB = 20;          // partial statistics loaded per batch (group sizes up to 20: one)
 
 template <int D>
@@ -48,8 +52,8 @@ struct Geo {
   static constexpr int KB = D / 64;           // 128-byte k-blocks per row
   static constexpr int KBLK = TILE * 128;     // bytes of one k-block of a 128-row tile
   static constexpr int TILE_BYTES = KB * KBLK;
-  static constexpr int OFF_Q = 0;             // 2 Q tiles
-  static constexpr int OFF_K = 2 * TILE_BYTES;
+  static constexpr int OFF_Q = 0;             // NQ Q tiles
+  static constexpr int OFF_K = NQ * TILE_BYTES;
   static constexpr int OFF_CTRL = OFF_K + NSTAGE * TILE_BYTES;
   static constexpr int CTRL_BYTES = 8192;
   static constexpr int NEED = OFF_CTRL + CTRL_BYTES + 1024;  // + base alignment slack
@@ -59,16 +63,17 @@ struct Geo {
 };
 
 // control-region byte offsets
-constexpr int C_QFULL = 0;      // 2 barriers
-constexpr int C_QEMPTY = 16;    // 2
-constexpr int C_KFULL = 32;     // NSTAGE
-constexpr int C_KEMPTY = 64;    // NSTAGE
-constexpr int C_SFULL = 96;     // 4 (TMEM accumulators)
-constexpr int C_SEMPTY = 128;   // 4
-constexpr int C_XFULL = 160;    // 2 (local statistics hand-off, g == 1)
-constexpr int C_XEMPTY = 176;   // 2
-constexpr int C_TMEM = 192;
-constexpr int C_ABORT = 196;
+constexpr int C_QFULL = 0;      // NQ (<= 4) barriers
+constexpr int C_QEMPTY = 32;    // NQ
+constexpr int C_KFULL = 64;     // NSTAGE (<= 4)
+constexpr int C_KEMPTY = 96;    // NSTAGE
+constexpr int C_SFULL = 128;    // 4 (TMEM accumulators)
+constexpr int C_SEMPTY = 160;   // 4
+constexpr int C_XFULL = 192;    // 2 (local statistics hand-off, g == 1)
+constexpr int C_XEMPTY = 208;   // 2
+constexpr int C_TMEM = 224;
+constexpr int C_ABORT = 228;
+static_assert(NQ <= 4 && NSTAGE <= 4, "barrier slots");
 constexpr int C_XSTAT = 256;    // float2 [2][128]  (2048 B)
 constexpr int C_OFF = 2304;     // float [128] (16-byte aligned: read as float4)
 constexpr int C_ROWPOS = 2816;  // int [128]
@@ -232,9 +237,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NQ; ++i) {
       mbar_init(ctl + C_QFULL + 8 * i, 1);
       mbar_init(ctl + C_QEMPTY + 8 * i, 2);  // both passes release the Q tile
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(ctl + C_XFULL + 8 * i, 4);
       mbar_init(ctl + C_XEMPTY + 8 * i, 4);
     }
@@ -263,25 +270,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   const int gamma = blockIdx.x / p.g, xg = blockIdx.x - gamma * p.g;
-  const int njobs = gamma < p.jobs ? (p.jobs - gamma + p.ngroups - 1) / p.ngroups : 0;
+  // CTAs past the last whole group (when g does not divide the grid) have no jobs
+  const int njobs = (gamma < p.ngroups && gamma < p.jobs) ? (p.jobs - gamma + p.ngroups - 1) / p.ngroups : 0;
 
   volatile int *tag = reinterpret_cast<volatile int *>(ctrl + C_TAG);
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
-      int kit = 0, qcnt[2] = {0, 0};
+      int kit = 0, qcnt[NQ] = {};
       bool ok = true;
-      Job Jb{};
-      for (int k = 0; k <= njobs && ok; ++k) {
-        Job Ja{};
+      for (int k = 0; k < njobs + LAG && ok; ++k) {
+        Job Ja{}, Jb{};
         int na = 0, nb = 0;
         if (k < njobs) {
           Ja = job_geo(p, gamma + k * p.ngroups, xg);
           na = Ja.t1 - Ja.t0;
         }
-        if (k >= 1) nb = Jb.t1 - Jb.t0;
-        if (na > 0) {  // Q tile of job k into buffer k & 1
-          const int qb = k & 1;
+        if (k >= LAG) {
+          Jb = job_geo(p, gamma + (k - LAG) * p.ngroups, xg);
+          nb = Jb.t1 - Jb.t0;
+        }
+        if (na > 0) {  // Q tile of job k into buffer k % NQ
+          const int qb = k % NQ;
           if (!ab.wait(ctl + C_QEMPTY + 8 * qb, (qcnt[qb] & 1) ^ 1)) { ok = false; break; }
           mbar_arrive_expect_tx(ctl + C_QFULL + 8 * qb, G::TILE_BYTES);
           for (int kb = 0; kb < G::KB; ++kb)
@@ -289,10 +299,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         Ja.u * p.R + Ja.rho0, ctl + C_QFULL + 8 * qb);
           ++qcnt[qb];
         }
+        if (PF > 0 && k == 0)  // the first pass-1 tiles of the first job
+          for (int i = 0; i < PF && i < na; ++i)
+            for (int kb = 0; kb < G::KB; ++kb) tma_prefetch_l2_2d(&tk, kb * 64, Ja.u * p.L + (Ja.t0 + i) * TILE);
         for (int ia = 0, ib = 0; ia < na || ib < nb;) {
           int row;
           if (next_is_a(ia, ib, na, nb)) {
             row = Ja.u * p.L + (Ja.t0 + ia) * TILE;
+            if (PF > 0) {  // keep the pass-1 stream PF tiles ahead in L2 (into the next job)
+              int pr = -1;
+              if (ia + PF < na) {
+                pr = Ja.u * p.L + (Ja.t0 + ia + PF) * TILE;
+              } else if (k + 1 < njobs) {
+                const Job Jn = job_geo(p, gamma + (k + 1) * p.ngroups, xg);
+                if (ia + PF - na < Jn.t1 - Jn.t0) pr = Jn.u * p.L + (Jn.t0 + ia + PF - na) * TILE;
+              }
+              if (pr >= 0)
+                for (int kb = 0; kb < G::KB; ++kb) tma_prefetch_l2_2d(&tk, kb * 64, pr);
+            }
             ++ia;
           } else {
             row = Jb.u * p.L + (Jb.t1 - 1 - ib) * TILE;
@@ -307,14 +331,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         ctl + C_KFULL + 8 * s);
           ++kit;
         }
-        Jb = Ja;
       }
       // drain: every issued copy must have landed before the CTA may exit
       for (int s = 0; s < NSTAGE; ++s) {
         const int cnt = kit / NSTAGE + (s < kit % NSTAGE ? 1 : 0);
         if (cnt > 0) mbar_wait_bounded(ctl + C_KFULL + 8 * s, (cnt - 1) & 1, p.timeout);
       }
-      for (int qb = 0; qb < 2; ++qb)
+      for (int qb = 0; qb < NQ; ++qb)
         if (qcnt[qb] > 0) mbar_wait_bounded(ctl + C_QFULL + 8 * qb, (qcnt[qb] - 1) & 1, p.timeout);
     }
   } else if (warp == 1 || warp == NWARPS - 1) {
@@ -324,20 +347,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // never holds up pass 1.
     if (lane == 0) {
       const bool mine_a = warp == 1;
-      int kit = 0, it = 0, last_bar = -1, last_par = 0, qcnt[2] = {0, 0};
+      int kit = 0, it = 0, last_bar = -1, last_par = 0, qcnt[NQ] = {};
       bool ok = true;
-      Job Jb{};
-      for (int k = 0; k <= njobs && ok; ++k) {
-        Job Ja{};
+      for (int k = 0; k < njobs + LAG && ok; ++k) {
+        Job Ja{}, Jb{};
         int na = 0, nb = 0;
         if (k < njobs) {
           Ja = job_geo(p, gamma + k * p.ngroups, xg);
           na = Ja.t1 - Ja.t0;
         }
-        if (k >= 1) nb = Jb.t1 - Jb.t0;
-        // this issuer's job of the round (pass 1: job k, pass 2: job k-1) and its Q buffer
+        if (k >= LAG) {
+          Jb = job_geo(p, gamma + (k - LAG) * p.ngroups, xg);
+          nb = Jb.t1 - Jb.t0;
+        }
+        // this issuer's job of the round (pass 1: job k, pass 2: job k - LAG), its Q buffer
         const int nmine = mine_a ? na : nb;
-        const int qb = (mine_a ? k : k - 1) & 1;
+        const int qb = (mine_a ? k : k - LAG + NQ) % NQ;
         if (nmine > 0) {
           if (!ab.wait(ctl + C_QFULL + 8 * qb, qcnt[qb] & 1)) { ok = false; break; }
           ++qcnt[qb];
@@ -379,7 +404,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (!ok) break;
         if (nmine > 0) umma_commit(ctl + C_QEMPTY + 8 * qb);  // this pass is done with the Q tile
-        Jb = Ja;
       }
       // drain: wait for the completion of the last MMA batch issued
       if (last_bar >= 0) mbar_wait_bounded(ctl + C_SFULL + 8 * last_bar, last_par, p.timeout);
