@@ -318,6 +318,15 @@ class H2OState:
         return H2OStateC(self.k.data_ptr(), self.v.data_ptr(), self.score.data_ptr(),
                          self.pos.data_ptr(), self.n_used.data_ptr(), self.free_slot.data_ptr())
 
+    def layer(self, l):
+        """A view of layer l alone (the state of a one-layer call, e.g. a layer-by-layer
+        prefill); it shares memory with this state."""
+        view = H2OState.__new__(H2OState)
+        view.n_heavy, view.n_recent, view.slots = self.n_heavy, self.n_recent, self.slots
+        for name in ("k", "v", "score", "pos", "n_used", "free_slot"):
+            setattr(view, name, getattr(self, name)[l:l + 1])
+        return view
+
 
 def _h2o_params(q, state, Hkv_from):
     Ly, B, Hq, D = q.shape[0], q.shape[1], q.shape[2], q.shape[-1]

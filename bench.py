@@ -240,6 +240,158 @@ def config_dict():
 # GPU arm
 # ------------------------------------------------------------------------------------
 
+def _events_ms(fn, n, warm):
+    """Median-free mean of n timed calls of fn (CUDA events on the current stream)."""
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n
+
+
+def measure_long(kvc, WL, dev, hbm_peak):
+    """Long-context SnapKV (batch 1, 8 layers, 32 MHA heads, L 131072, budget 1024): one
+    compression of all layers, then 128 decode steps with the fused append."""
+    import torch
+    w = WL.LONG
+    x = WL.snapkv_prompt(w, WL.seed_of(3), dev)
+    Ly, Bb, H, Dd, Ll, Wn, Kb, S = w.layers, w.batch, w.kv_heads, w.head_dim, w.prompt_len, \
+        w.window, w.budget, w.decode_steps
+    cap = Kb + S
+    kc = torch.empty((Ly, Bb, H, cap, Dd), dtype=torch.bfloat16, device=dev)
+    vc, pos = torch.empty_like(kc), torch.empty((Ly, Bb, H, cap), dtype=torch.int32, device=dev)
+    nv = torch.empty((Ly, Bb, H), dtype=torch.int32, device=dev)
+
+    def compress():
+        kvc.snapkv_compress(x["Q_win"], x["K"], x["V"], keep_window=Wn, pool_kernel=w.pool_kernel,
+                            budget=Kb, cap=cap, k_out=kc, v_out=vc, pos_out=pos, n_valid_out=nv)
+
+    c_ms = _events_ms(compress, 5, 3)
+    per = (w.q_heads * Wn * Dd * 2 + H * Ll * Dd * 2 + 8 * H * (Ll - Wn) + 8 * H * Kb * Dd + 4 * H * Kb)
+    c_bytes = per * Ly * Bb
+    dec = [WL.decode_token(w, s, WL.seed_of(3, 100), dev) for s in range(8)]
+    out = torch.empty((Ly, Bb, w.q_heads, Dd), dtype=torch.bfloat16, device=dev)
+    compress()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for s in range(S):
+        q, kn, vn = dec[s % 8]
+        kvc.compressed_decode_attn(q, kc, vc, n_valid=nv, n_uniform=Kb + s + 1, k_new=kn, v_new=vn,
+                                   pos=pos, new_pos=Ll + s, out=out)
+    b.record()
+    torch.cuda.synchronize()
+    d_ms = a.elapsed_time(b) / S
+    d_bytes = sum(Ly * Bb * (4 * H * (Kb + s + 1) * Dd + 4 * w.q_heads * Dd + 4 * H * Dd)
+                  for s in range(S)) / S
+    status = kvc.kvc_device_status()
+    del x, kc, vc
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "compress_ms": c_ms, "prefix_tokens_per_s": Bb * Ll / (c_ms / 1e3),
+            "compress_GBps": c_bytes / (c_ms / 1e3) / 1e9,
+            "compress_frac_of_hbm_peak": c_bytes / (c_ms / 1e3) / 1e9 / hbm_peak,
+            "decode_ms_per_step": d_ms, "decode_GBps": d_bytes / (d_ms / 1e3) / 1e9,
+            "decode_frac_of_hbm_peak": d_bytes / (d_ms / 1e3) / 1e9 / hbm_peak,
+            "decode_launch": "eager, one call per step for all layers", "device_status": status}
+
+
+def measure_h2o(kvc, WL, dev, hbm_peak, steps=64):
+    """H2O on OPT-6.7B shapes (batch 64, 32 layers, 32 MHA heads, prompt 2048, 204 heavy +
+    204 recent): layer-by-layer prefill (scores + cut), then decode steps of all layers."""
+    import torch
+    w = WL.H2O_OPT
+    Ly, Bb, H, Dd = w.layers, w.batch, w.kv_heads, w.head_dim
+    st = kvc.H2OState(Ly, Bb, H, Dd, w.n_heavy, w.n_recent, dev)
+    pre_ms = []
+    for l in range(Ly):
+        Q, K, V = WL.h2o_prompt_layer(w, l, WL.seed_of(4), dev)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        kvc.h2o_prefill(Q[None], K[None], V[None], n_heavy=w.n_heavy, n_recent=w.n_recent,
+                        state=st.layer(l))
+        b.record()
+        torch.cuda.synchronize()
+        pre_ms.append(a.elapsed_time(b))
+        del Q, K, V
+    torch.cuda.empty_cache()
+    toks = [WL.decode_token(w, s, WL.seed_of(4, 100), dev) for s in range(4)]
+    out = torch.empty((Ly, Bb, w.q_heads, Dd), dtype=torch.bfloat16, device=dev)
+    ev = torch.empty((Ly, Bb, H), dtype=torch.int32, device=dev)
+    t0 = w.prompt_len
+    for s in range(4):  # warm-up steps
+        q, kn, vn = toks[s]
+        kvc.h2o_decode_step(q, kn, vn, st, t0 + s, out=out, evicted=ev)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for s in range(steps):
+        q, kn, vn = toks[s % 4]
+        kvc.h2o_decode_step(q, kn, vn, st, t0 + 4 + s, out=out, evicted=ev)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    n = w.n_heavy + w.n_recent + 1
+    step_bytes = Ly * Bb * H * (n * (4 * Dd + 12) + 4 * (w.q_heads // H) * Dd + 4 * Dd)
+    status = kvc.kvc_device_status()
+    del st
+    torch.cuda.empty_cache()
+    # causal Q.K^T flops of the prefill scores (half the square) per layer
+    pre_flops = 2.0 * Bb * w.q_heads * w.prompt_len * w.prompt_len / 2 * Dd
+    return {"workload": w.name, "prefill_ms_per_layer": statistics.median(pre_ms),
+            "prefill_causal_qk_TFLOPs": pre_flops / (statistics.median(pre_ms) / 1e3) / 1e12,
+            "step_ms": ms, "step_GBps": step_bytes / (ms / 1e3) / 1e9,
+            "step_frac_of_hbm_peak": step_bytes / (ms / 1e3) / 1e9 / hbm_peak,
+            "steps_timed": steps, "device_status": status}
+
+
+def measure_stream(kvc, WL, dev, hbm_peak, steps=256):
+    """StreamingLLM on Llama-2-13B shapes (batch 16, 40 layers, 40 MHA heads, 4 sinks +
+    2044-token ring): fill the cache, then steady-state steps of append + attention."""
+    import torch
+    w = WL.STREAM
+    Ly, Bb, H, Dd, S, R = w.layers, w.batch, w.kv_heads, w.head_dim, w.n_sink, w.ring
+    kc = torch.zeros((Ly, Bb, H, S + R, Dd), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    pos = torch.full((Ly, Bb, H, S + R), -1, dtype=torch.int32, device=dev)
+    toks = [WL.stream_token(w, t, WL.seed_of(5), dev) for t in range(8)]
+    for t in range(S + R):
+        _, k, v = toks[t % 8]
+        kvc.sink_window_append(k, v, kc, vc, t, n_sink=S, n_recent=R, pos=pos)
+    out = torch.empty((Ly, Bb, w.q_heads, Dd), dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+    t0 = S + R
+
+    def step(t):
+        q, k, v = toks[t % 8]
+        kvc.sink_window_append(k, v, kc, vc, t, n_sink=S, n_recent=R, pos=pos)
+        kvc.compressed_decode_attn(q, kc, vc, n_uniform=S + R, out=out)
+
+    for t in range(t0, t0 + 4):
+        step(t)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(steps):
+        step(t0 + 4 + i)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    step_bytes = Ly * Bb * (4 * H * (S + R) * Dd + 4 * w.q_heads * Dd + 4 * H * Dd + 4 * H)
+    status = kvc.kvc_device_status()
+    del kc, vc
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "step_ms": ms, "step_GBps": step_bytes / (ms / 1e3) / 1e9,
+            "step_frac_of_hbm_peak": step_bytes / (ms / 1e3) / 1e9 / hbm_peak,
+            "steps_timed": steps, "launches_per_step": 2, "device_status": status}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -431,6 +583,13 @@ def run_ours(args):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if rank == 0 and not args.no_aux:
+        # the other configurations of the hot path, measured after the headline
+        del Q, K, V, x, kc, vc, graph
+        torch.cuda.empty_cache()
+        line["aux"] = {"long_context": measure_long(kvc, WL, dev, hbm_peak),
+                       "h2o": measure_h2o(kvc, WL, dev, hbm_peak),
+                       "streaming": measure_stream(kvc, WL, dev, hbm_peak)}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
@@ -448,6 +607,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-aux", action="store_true",
+                    help="skip the long-context, H2O and streaming measurements")
     ap.add_argument("--layers", type=int, default=32, help="profiling only: fewer layers")
     ap.add_argument("--decode-steps", type=int, default=256, help="profiling only")
     args = ap.parse_args()
