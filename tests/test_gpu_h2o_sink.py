@@ -13,6 +13,55 @@ from parity import BAND, assert_outputs_close, assert_votes_close, check_selecte
 pytestmark = pytest.mark.gpu
 
 
+def check_prefill_unit(q, K, V, gpu_pos, gpu_score, n_heavy, n_recent):
+    """One unit's prefill cut and scores against the oracle (fp64 q [G,L,D], K, V [L,D]).
+    Returns (oracle state that follows the GPU's cut, number of in-band swaps)."""
+    L, D = K.shape
+    o = OH.prefill(q, K, V, n_heavy, n_recent)
+    n_keep = min(L, n_heavy + n_recent)
+    gp = gpu_pos[:n_keep]
+    assert (gpu_pos[n_keep:] == -1).all()
+    swaps = 0
+    if L > n_heavy + n_recent:
+        from oracle.snapkv import window_votes
+        full = window_votes(q, K)
+        assert list(gp[n_heavy:]) == list(range(L - n_recent, L))
+        if n_heavy:
+            swaps += check_selected_set(gp[:n_heavy], np.sort(o.pos[:n_heavy]), full[:L - n_recent],
+                                        n_heavy)
+        if set(gp) != set(o.pos[:n_keep].tolist()):
+            # follow the GPU's equally valid cut: rebuild the oracle state from it
+            o = OH.H2OState(n_heavy + n_recent + 1, D)
+            o.k[:n_keep], o.v[:n_keep] = K[gp], V[gp]
+            o.score[:n_keep], o.pos[:n_keep] = full[gp], gp
+            o.n_used = o.free_slot = n_keep
+    # scores of the kept entries (slot order may differ: compare by position)
+    ref_by_pos = {int(p): s for p, s in zip(o.pos[:o.n_used], o.score[:o.n_used])}
+    assert_votes_close(gpu_score[:n_keep], [ref_by_pos[int(p)] for p in gp], "prefill scores")
+    return o, swaps
+
+
+def check_step_unit(o, q, k_new, v_new, t, n_recent, gpu_out, gpu_evicted, gpu_pos, what):
+    """One unit's decode step against the oracle state o (advanced in place).  If the GPU
+    evicted a different entry, it must be an equally valid choice (score within the band
+    of the minimum); the oracle then follows it.  Returns the number of such swaps."""
+    snap = (o.k.copy(), o.v.copy(), o.score.copy(), o.pos.copy(), o.n_used, o.free_slot)
+    ro, rev, cand = OH.step(o, q, k_new, v_new, t, n_recent)
+    assert_outputs_close(gpu_out, ro, what)
+    swaps = 0
+    if int(gpu_evicted) != rev:
+        best = min(c[2] for c in cand)
+        gsel = [c for c in cand if c[1] == int(gpu_evicted)]
+        assert gsel and abs(gsel[0][2] - best) <= BAND * abs(best), (
+            "%s: evicted %d, oracle %d" % (what, gpu_evicted, rev))
+        o.k, o.v, o.score, o.pos, o.n_used, o.free_slot = snap
+        o.k, o.v, o.score, o.pos = (a.copy() for a in (o.k, o.v, o.score, o.pos))
+        OH.step(o, q, k_new, v_new, t, n_recent, evict_override=gsel[0][0])
+        swaps = 1
+    assert set(gpu_pos[gpu_pos >= 0].tolist()) - {int(gpu_evicted)} == set(o.pos[o.live()].tolist())
+    return swaps
+
+
 def run_h2o_lockstep(kvc, Ly, B, Hq, Hkv, D, L, n_heavy, n_recent, steps, seed):
     g = torch.Generator().manual_seed(seed)
     Q = torch.randn((Ly, B, Hq, L, D), generator=g).to(torch.bfloat16)
@@ -30,28 +79,10 @@ def run_h2o_lockstep(kvc, Ly, B, Hq, Hkv, D, L, n_heavy, n_recent, steps, seed):
     pos = st.pos.cpu().numpy()
     score = st.score.cpu().numpy()
     for (ly, b, h) in units:
-        o = OH.prefill(Qh[ly, b, h * G:(h + 1) * G], Kh[ly, b, h], Vh[ly, b, h], n_heavy, n_recent)
-        n_keep = min(L, n_heavy + n_recent)
-        gp = pos[ly, b, h, :n_keep]
-        assert (pos[ly, b, h, n_keep:] == -1).all()
-        if L > n_heavy + n_recent:
-            from oracle.snapkv import window_votes
-            full = window_votes(Qh[ly, b, h * G:(h + 1) * G], Kh[ly, b, h])
-            assert list(gp[n_heavy:]) == list(range(L - n_recent, L))
-            if n_heavy:
-                swaps += check_selected_set(gp[:n_heavy], np.sort(o.pos[:n_heavy]),
-                                            full[:L - n_recent], n_heavy)
-            if set(gp) != set(o.pos[:n_keep].tolist()):
-                # follow the GPU's equally valid cut: rebuild the oracle state from it
-                o = OH.H2OState(n_heavy + n_recent + 1, D)
-                o.k[:n_keep], o.v[:n_keep] = Kh[ly, b, h, gp], Vh[ly, b, h, gp]
-                o.score[:n_keep], o.pos[:n_keep] = full[gp], gp
-                o.n_used = o.free_slot = n_keep
-        # scores of the kept entries (slot order may differ: compare by position)
-        ref_by_pos = {int(p): s for p, s in zip(o.pos[:o.n_used], o.score[:o.n_used])}
-        assert_votes_close(score[ly, b, h, :n_keep], [ref_by_pos[int(p)] for p in gp],
-                           "prefill scores")
-        ref[(ly, b, h)] = o
+        ref[(ly, b, h)], sw = check_prefill_unit(Qh[ly, b, h * G:(h + 1) * G], Kh[ly, b, h],
+                                                 Vh[ly, b, h], pos[ly, b, h], score[ly, b, h],
+                                                 n_heavy, n_recent)
+        swaps += sw
     for s in range(steps):
         t = L + s
         q = torch.randn((Ly, B, Hq, D), generator=g).to(torch.bfloat16)
@@ -62,26 +93,12 @@ def run_h2o_lockstep(kvc, Ly, B, Hq, Hkv, D, L, n_heavy, n_recent, steps, seed):
         assert kvc.kvc_device_status() == 0
         outh, evh = f64(out), ev.cpu().numpy()
         gpu_pos = st.pos.cpu().numpy()
+        qh, knh, vnh = f64(q), f64(kn), f64(vn)
         for (ly, b, h) in units:
-            o = ref[(ly, b, h)]
-            qh = f64(q)[ly, b, h * G:(h + 1) * G]
-            # run the oracle step; if the GPU evicted a different entry, it must be an
-            # equally valid choice (score within the band of the minimum), then follow it
-            snap = (o.k.copy(), o.v.copy(), o.score.copy(), o.pos.copy(), o.n_used, o.free_slot)
-            ro, rev, cand = OH.step(o, qh, f64(kn)[ly, b, h], f64(vn)[ly, b, h], t, n_recent)
-            assert_outputs_close(outh[ly, b, h * G:(h + 1) * G], ro, "h2o step %d" % s)
-            if int(evh[ly, b, h]) != rev:
-                best = min(c[2] for c in cand)
-                gsel = [c for c in cand if c[1] == int(evh[ly, b, h])]
-                assert gsel and abs(gsel[0][2] - best) <= BAND * abs(best), (
-                    "step %d unit %s: evicted %d, oracle %d" % (t, (ly, b, h), evh[ly, b, h], rev))
-                o.k, o.v, o.score, o.pos, o.n_used, o.free_slot = snap
-                o.k, o.v, o.score, o.pos = (a.copy() for a in (o.k, o.v, o.score, o.pos))
-                OH.step(o, qh, f64(kn)[ly, b, h], f64(vn)[ly, b, h], t, n_recent,
-                        evict_override=gsel[0][0])
-                swaps += 1
-            assert set(gpu_pos[ly, b, h][gpu_pos[ly, b, h] >= 0].tolist()) - {int(evh[ly, b, h])} \
-                == set(o.pos[o.live()].tolist())
+            swaps += check_step_unit(ref[(ly, b, h)], qh[ly, b, h * G:(h + 1) * G], knh[ly, b, h],
+                                     vnh[ly, b, h], t, n_recent, outh[ly, b, h * G:(h + 1) * G],
+                                     evh[ly, b, h], gpu_pos[ly, b, h],
+                                     "h2o step %d unit %s" % (t, (ly, b, h)))
     return swaps
 
 
