@@ -189,6 +189,12 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
     fence_mbar_init();
   }
   __syncthreads();
+  // Programmatic dependent launch: the next kernel of the stream may start launching
+  // now (its CTAs take SM slots as this grid's CTAs exit, and wait here until this grid
+  // has completed); this grid waits for the previous kernel before reading anything
+  // it wrote (q, the caches, n_valid, the workspace counters).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     // ------ TMA producer: per segment its q, then per sub-chunk K tiles, V tiles ------
@@ -543,8 +549,17 @@ cudaError_t launch_t(const Ctx &c, const DecodeArgs &a, DecP p) {
   long long grid = (long long)c.num_sms * (dev < 64 ? per_sm[dev] : 1);
   if (grid > slots) grid = slots;
   if (grid < 1) grid = 1;
-  decode_kernel<D, G><<<(unsigned)grid, NTH, DGeo<D, G>::SMEM, c.stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(NTH);
+  cfg.dynamicSmemBytes = DGeo<D, G>::SMEM;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddepcontrol above
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, G>, tk, tv, p);
 }
 
 }  // namespace

@@ -44,7 +44,6 @@ constexpr int NWARPS = 19;      // TMA, pass-1 MMA, 8 pass-1 warps, 8 pass-2 war
 constexpr int NTHREADS = 32 * NWARPS;
 constexpr int TMEM_COLS = 512;  // 4 accumulators of 128 fp32 columns
 constexpr int LEAD = 2;         // pass-1 tiles of a round issued before its first pass-2 tile
-constexpr int PF = 0;           // pass-1 tiles prefetched into L2 ahead of the ring
 constexpr int XB = 20;          // partial statistics loaded per batch (group sizes up to 20: one)
 
 template <int D>
@@ -299,24 +298,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         Ja.u * p.R + Ja.rho0, ctl + C_QFULL + 8 * qb);
           ++qcnt[qb];
         }
-        if (PF > 0 && k == 0)  // the first pass-1 tiles of the first job
-          for (int i = 0; i < PF && i < na; ++i)
-            for (int kb = 0; kb < G::KB; ++kb) tma_prefetch_l2_2d(&tk, kb * 64, Ja.u * p.L + (Ja.t0 + i) * TILE);
         for (int ia = 0, ib = 0; ia < na || ib < nb;) {
           int row;
           if (next_is_a(ia, ib, na, nb)) {
             row = Ja.u * p.L + (Ja.t0 + ia) * TILE;
-            if (PF > 0) {  // keep the pass-1 stream PF tiles ahead in L2 (into the next job)
-              int pr = -1;
-              if (ia + PF < na) {
-                pr = Ja.u * p.L + (Ja.t0 + ia + PF) * TILE;
-              } else if (k + 1 < njobs) {
-                const Job Jn = job_geo(p, gamma + (k + 1) * p.ngroups, xg);
-                if (ia + PF - na < Jn.t1 - Jn.t0) pr = Jn.u * p.L + (Jn.t0 + ia + PF - na) * TILE;
-              }
-              if (pr >= 0)
-                for (int kb = 0; kb < G::KB; ++kb) tma_prefetch_l2_2d(&tk, kb * 64, pr);
-            }
             ++ia;
           } else {
             row = Jb.u * p.L + (Jb.t1 - 1 - ib) * TILE;
