@@ -10,24 +10,29 @@
 // * persistent stream-K: all units' 64-row tile slots form one sequence that is split
 //   evenly over a grid of resident CTAs (three per SM), so every CTA streams the same
 //   number of tiles; a CTA's range covers segments of one or more units.  Warp 0
-//   streams each segment's K tiles and then its V tiles through one continuous 3-stage
+//   streams each segment's tiles as K0, V0, K1, V1, ... through one continuous 4-stage
 //   shared-memory ring with TMA (128-byte swizzle, one mbarrier pair per stage), so the
 //   next segment's loads overlap the current segment's epilogue; warps 1-4 compute.
-// * K phase: D/8 threads per row, each owning one 16-byte chunk (8 head dims) of every
-//   row (conflict-free reads of the swizzled tile); the thread's slice of q, pre-scaled
-//   by log2(e)/sqrt(D), lives in registers (a bulk copy brings each unit's q to shared
+//   The throughput of a CTA is the bytes in flight over the memory latency, so the
+//   shared memory goes to the ring: no logit buffer, no block-wide softmax.
+// * each compute warp owns 16 rows of every tile, in both halves of the step, and keeps
+//   its own online softmax (running max, normaliser and o per head; FlashAttention's
+//   rescaling), so a tile needs no synchronisation between the warps.
+// * K half: D/8 threads per row, each owning one 16-byte chunk (8 head dims) of the row
+//   (conflict-free reads of the swizzled tile); the thread's slice of q, pre-scaled by
+//   log2(e)/sqrt(D), lives in registers (a bulk copy brings each unit's q to shared
 //   memory ahead of time); packed fp32x2 FMA; a transpose-reduce over the row's lanes
-//   leaves one head's logit per lane; the logits of the chunk go to shared memory.
-// * one block reduction per chunk gives each head's maximum and normaliser; the logits
-//   become exp2(s - max) in place (chunks of a long segment are merged with a running
-//   maximum, rescaling the sums kept in registers).
-// * V phase: lanes over the head dim, each warp over 16 rows of a tile, packed FMA
-//   with the stored probabilities.  Rows at or past n are never touched.
-// * the four warps' sums merge in shared memory; a unit covered by one segment is
-//   written directly, otherwise each segment's (max, normaliser, o) goes to the
-//   workspace and the last CTA to finish one of the unit's segments (atomic counter,
-//   no waiting) merges them and writes the bf16 output, resetting the counter.  The counters live in a fixed 256 KB header of the workspace (one int per
-//   unit, at most 65535 units) that is zero between calls, whatever the call shapes.
+//   leaves one head's logit per lane.  The warp's 16 probabilities per head go through
+//   a small per-warp buffer to every lane.
+// * V half: lanes over the head dim, packed FMA with those probabilities.  Rows at or
+//   past n are never touched.
+// * at the end of a segment the four warps' (max, normaliser, o) merge in shared
+//   memory; a unit covered by one segment is written directly, otherwise each
+//   segment's (max, normaliser, o) goes to the workspace and the last CTA to finish one
+//   of the unit's segments (atomic counter, no waiting) merges them and writes the bf16
+//   output, resetting the counter.  The counters live in a fixed 256 KB header of the
+//   workspace (one int per unit, at most 65535 units) that is zero between calls,
+//   whatever the call shapes.
 #include <math.h>
 
 #include "kvc_internal.cuh"
@@ -36,8 +41,9 @@ namespace kvc {
 namespace {
 
 constexpr int ROWS = 64;     // rows per tile
-constexpr int NST = 3;       // ring depth (K or V tiles)
+constexpr int NST = 4;       // ring depth (K or V tiles)
 constexpr int NCW = 4;       // compute warps
+constexpr int WROWS = ROWS / NCW;  // rows of a tile per compute warp
 constexpr int NTH = 32 * (NCW + 1);
 
 template <int D, int G>
@@ -45,18 +51,20 @@ struct DGeo {
   static constexpr int KB = D / 64;
   static constexpr int KBLK = ROWS * 128;        // bytes of one k-block of a tile
   static constexpr int TB = KB * KBLK;           // bytes of one K or V tile
-  static constexpr int CMAX = 4096 / G;          // rows of one chunk (logits = 16 KB)
   static constexpr int QB = G * D * 2;           // bytes of one unit's q (bf16)
   static constexpr int OFF_RING = 0;
-  static constexpr int OFF_LOG = NST * TB;                   // fp32 [CMAX][G]; the merge
-                                                             // buffer [NCW][G][D] reuses it
-  static constexpr int OFF_QB = OFF_LOG + CMAX * G * 4;      // bf16 [2][G][D]
-  static constexpr int OFF_ST = OFF_QB + 2 * QB;             // fp32 [NCW][G]
-  static constexpr int OFF_BAR = OFF_ST + NCW * G * 4 + 64;
+  static constexpr int OFF_QB = NST * TB;                    // bf16 [2][G][D]
+  static constexpr int OFF_P = OFF_QB + 2 * QB;              // fp32 [NCW][WROWS][G] probabilities
+  static constexpr int OFF_RED = OFF_P + NCW * WROWS * G * 4;  // fp32 [G][D] merged o
+  static constexpr int OFF_WX = OFF_RED + G * D * 4;         // fp32 [NCW][G] tile max / sum
+  static constexpr int OFF_ST = OFF_WX + NCW * G * 4;        // float2 [NCW][G] (max, normaliser)
+  static constexpr int OFF_BAR = OFF_ST + NCW * G * 8;
   static constexpr int SMEM = OFF_BAR + 128 + 1024;
-  static constexpr int DV = D / 32;              // head-dim elements per lane in the V phase
-  static constexpr int TPR = D / 8;              // K phase: threads per row, one chunk each
-  static_assert(NCW * G * D * 4 <= CMAX * G * 4, "merge buffer must fit the logit buffer");
+  static constexpr int DV = D / 32;              // head-dim elements per lane in the V half
+  static constexpr int TPR = D / 8;              // K half: threads per row, one chunk each
+  static constexpr int RPW = 32 / TPR;           // K half: rows per warp and pass
+  static constexpr int NPASS = WROWS / RPW;      // K half: passes over the warp's rows
+  static_assert(G <= TPR, "every head's logit needs a lane of the row");
 };
 
 struct DecP {
@@ -152,6 +160,7 @@ __device__ __forceinline__ Seg seg_geo(const DecP &p, int u, int b, int s0, int 
   return g;
 }
 
+
 template <int D, int G>
 __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ CUtensorMap tk,
                                                      const __grid_constant__ CUtensorMap tv,
@@ -161,9 +170,9 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
-  float *slog = reinterpret_cast<float *>(smem + Gm::OFF_LOG);  // [row][G]
-  float *red = slog;  // merge buffer, used only after a segment's V phase
-  float *wst = reinterpret_cast<float *>(smem + Gm::OFF_ST);    // [NCW][G] per-warp partials
+  float *red = reinterpret_cast<float *>(smem + Gm::OFF_RED);   // [G][D] merged o
+  float *wx = reinterpret_cast<float *>(smem + Gm::OFF_WX);     // [NCW][G] tile max / sum
+  float2 *wst = reinterpret_cast<float2 *>(smem + Gm::OFF_ST);  // [NCW][G] (max, normaliser)
   // barriers: full[NST] at +0, empty[NST] at +32, qfull[2] at +64, qempty[2] at +80
   const uint32_t bar = sb + Gm::OFF_BAR;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Gm::OFF_BAR + 96);
@@ -176,6 +185,7 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
   const int s0 = slot_first(b, Q, R), s1 = slot_first(b + 1, Q, R);
   const int u_first = s0 / T, u_last = s1 > s0 ? (s1 - 1) / T : u_first - 1;
 
+  for (int e = threadIdx.x; e < G * D; e += NTH) red[e] = 0.f;
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int i = 0; i < NST; ++i) {
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
-    // ------ TMA producer: per segment its q, then per sub-chunk K tiles, V tiles ------
+    // ------ TMA producer: per segment its q, then its tiles as K0, V0, K1, V1, ... ------
     if (lane == 0) {
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
@@ -209,19 +219,16 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
         if (!ab.wait(bar + 80 + 8 * qb, ((k >> 1) & 1) ^ 1)) { ok = false; break; }
         mbar_arrive_expect_tx(bar + 64 + 8 * qb, Gm::QB);
         bulk_load(sb + Gm::OFF_QB + qb * Gm::QB, p.q + (size_t)u * G * D, Gm::QB, bar + 64 + 8 * qb);
-        for (int c0 = g.r0; c0 < g.r1 && ok; c0 += Gm::CMAX) {
-          const int ntiles = (min(g.r1, c0 + Gm::CMAX) - c0 + ROWS - 1) / ROWS;
-          for (int i = 0; i < 2 * ntiles; ++i, ++it) {
-            const int st = it % NST, use = it / NST;
-            if (!ab.wait(bar + 32 + 8 * st, (use & 1) ^ 1)) { ok = false; break; }
-            mbar_arrive_expect_tx(bar + 8 * st, Gm::TB);
-            const int tt = i < ntiles ? i : i - ntiles;
-            const int row = u * p.cap + c0 + tt * ROWS;
-            const CUtensorMap *map = i < ntiles ? &tk : &tv;
-            for (int kb = 0; kb < Gm::KB; ++kb)
-              tma_load_2d(sb + Gm::OFF_RING + st * Gm::TB + kb * Gm::KBLK, map, kb * 64, row,
-                          bar + 8 * st);
-          }
+        const int ntiles = (g.r1 - g.r0 + ROWS - 1) / ROWS;
+        for (int i = 0; i < 2 * ntiles; ++i, ++it) {
+          const int st = it % NST, use = it / NST;
+          if (!ab.wait(bar + 32 + 8 * st, (use & 1) ^ 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar + 8 * st, Gm::TB);
+          const int row = u * p.cap + g.r0 + (i >> 1) * ROWS;
+          const CUtensorMap *map = (i & 1) ? &tv : &tk;
+          for (int kb = 0; kb < Gm::KB; ++kb)
+            tma_load_2d(sb + Gm::OFF_RING + st * Gm::TB + kb * Gm::KBLK, map, kb * 64, row,
+                        bar + 8 * st);
         }
       }
       for (int st = 0; st < NST; ++st) {  // drain
@@ -237,12 +244,24 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
   }
 
   // ------------------------------ compute warps ------------------------------
-  const int cw = warp - 1;         // 0..3
+  const int cw = warp - 1;         // 0..3: owns rows [cw*WROWS, (cw+1)*WROWS) of every tile
   const int t = threadIdx.x - 32;  // 0..127
-  constexpr int TPR = Gm::TPR;
-  const int rg = lane / TPR;       // K phase: row within the warp's group of 32/TPR rows
-  const int sl = lane % TPR;       // K phase: the thread's 16-byte chunk of the row
-  constexpr int DV = Gm::DV;
+  constexpr int TPR = Gm::TPR, RPW = Gm::RPW, NPASS = Gm::NPASS, DV = Gm::DV;
+  constexpr int WMASK = TPR / G - 1;  // lanes of a row holding the same head's logit
+  const int rg = lane / TPR;          // K half: row within the warp's pass
+  const int sl = lane % TPR;          // K half: the thread's 16-byte chunk of the row
+  // the head whose logit this lane holds after the transpose-reduce (see below)
+  int myhead = 0;
+#pragma unroll
+  for (int lvl = TPR / 2, nv = G; lvl >= 1; lvl >>= 1)
+    if (nv >= 2) {
+      if (lane & lvl) myhead += nv / 2;
+      nv /= 2;
+    }
+  const bool row_writer = (lane & WMASK) == 0;        // one lane per (row, head)
+  const bool head_writer = row_writer && lane < TPR;  // one lane per head
+  float *pw = reinterpret_cast<float *>(smem + Gm::OFF_P) + cw * WROWS * G;  // [WROWS][G]
+  float *wxw = wx + cw * G;
   int it = 0, k = 0;
   bool ok = true;
   for (int u = u_first; u <= u_last; ++u, ++k) {
@@ -275,27 +294,30 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
 #pragma unroll
       for (int d = 0; d < DV / 2; ++d) o2[g][d] = 0ull;
     }
-    for (int c0 = sg.r0; c0 < sg.r1; c0 += Gm::CMAX) {
-      const int nrows = min(sg.r1, c0 + Gm::CMAX) - c0;
-      const int ntiles = (nrows + ROWS - 1) / ROWS;
-      const int arow_local = sg.arow - c0;
-      // ---- K phase: logits of the sub-chunk's rows (8 threads per row) ----
-      for (int i = 0; i < ntiles; ++i) {
-        const int j = it + i, st = j % NST;
-        const bool got = __all_sync(0xffffffffu, ok && ab.wait(bar + 8 * st, (j / NST) & 1));
+    const int nrows = sg.r1 - sg.r0;
+    const int ntiles = (nrows + ROWS - 1) / ROWS;
+    const int arow_local = sg.arow - sg.r0;
+    for (int i = 0; i < ntiles; ++i, it += 2) {
+      const int arr = arow_local - i * ROWS;
+      const bool patched = sg.arow >= 0 && arr >= 0 && arr < ROWS;  // same for the CTA
+      const int wrows = min(WROWS, nrows - i * ROWS - cw * WROWS);   // this warp's rows (<= 0: none)
+      // ---------------- K half: logits of the warp's rows ----------------
+      float lg[NPASS];
+      {
+        const int st = it % NST;
+        const bool got = __all_sync(0xffffffffu, ok && ab.wait(bar + 8 * st, (it / NST) & 1));
         ok = got;
         uint8_t *tile = smem + Gm::OFF_RING + st * Gm::TB;
-        const int arr = arow_local - i * ROWS;
-        const bool patched = sg.arow >= 0 && arr >= 0 && arr < ROWS;  // same for the CTA
         if (patched) {  // every compute thread reaches this barrier
           if (got) patch_row<D>(tile, p.k_new + (size_t)u * D, arr, t);
           named_bar(1, 128);
         }
+#pragma unroll
+        for (int pass = 0; pass < NPASS; ++pass) lg[pass] = -INFINITY;
         if (got) {
-          constexpr int RPW = 32 / TPR;  // rows per warp and pass
-#pragma unroll 2
-          for (int pass = 0; pass < ROWS / (NCW * RPW); ++pass) {
-            const int r = (pass * NCW + cw) * RPW + rg;  // row of the tile
+#pragma unroll
+          for (int pass = 0; pass < NPASS; ++pass) {
+            const int r = cw * WROWS + pass * RPW + rg;  // row of the tile
             // chunk sl: k-block sl / 8, slot sl % 8 (the 8 lanes of a phase hit 8 slots)
             const uint4 w = *reinterpret_cast<const uint4 *>(
                 tile + (sl >> 3) * Gm::KBLK + r * 128 + (((sl & 7) ^ (r & 7)) << 4));
@@ -313,8 +335,7 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
               v[g] = a.x + a.y;
             }
             // transpose-reduce over the row's TPR lanes: each split level halves the heads a
-            // lane keeps; afterwards the lane's high bits name the head it holds
-            int head = 0;
+            // lane keeps (the lane's bits at those levels name the head it keeps, myhead)
 #pragma unroll
             for (int lvl = TPR / 2, nv = G; lvl >= 1; lvl >>= 1) {
               if (nv >= 2) {
@@ -327,72 +348,53 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
                     v[x] = keep + __shfl_xor_sync(0xffffffffu, send, lvl);
                   }
                 }
-                if (upper) head += nv / 2;
                 nv /= 2;
               } else {
                 v[0] += __shfl_xor_sync(0xffffffffu, v[0], lvl);
               }
             }
-            const int row = i * ROWS + r;
-            constexpr int WMASK = TPR / G > 1 ? TPR / G - 1 : 0;
-            if ((lane & WMASK) == 0 && row < nrows) slog[row * G + head] = v[0];
+            if (pass * RPW + rg < wrows) lg[pass] = v[0];
           }
           if (patched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar + 32 + 8 * st);
+          if (lane == 0) mbar_arrive(bar + 32 + 8 * st);  // the K stage may be refilled
         }
       }
-      named_bar(1, 128);
-      // ---- sub-chunk max; new running max; p = exp2(s - max) in place; sums ----
+      // ------- online softmax of the warp's rows (no other warp is involved) -------
       float mnew[G], f[G];
       {
-        float mx[G];
+        float tmax = lg[0];
 #pragma unroll
-        for (int g = 0; g < G; ++g) mx[g] = -INFINITY;
-        for (int r = t; r < nrows; r += 128)
+        for (int pass = 1; pass < NPASS; ++pass) tmax = fmaxf(tmax, lg[pass]);
+        // lanes holding the same head differ in the row bits (lane / TPR)
 #pragma unroll
-          for (int g = 0; g < G; ++g) mx[g] = fmaxf(mx[g], slog[r * G + g]);
+        for (int o = TPR; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+        if (head_writer) wxw[myhead] = tmax;
+        __syncwarp();
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], o));
-          if (lane == 0) wst[cw * G + g] = mx[g];
+          mnew[g] = fmaxf(m_run[g], wxw[g]);
+          f[g] = m_run[g] == -INFINITY ? 0.f : ex2(m_run[g] - mnew[g]);  // rescale of the past
         }
-        named_bar(1, 128);
+        __syncwarp();  // wxw is reused for the sums
+        float mh = mnew[0];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float m2 = m_run[g];
+        for (int g = 1; g < G; ++g)
+          if (myhead == g) mh = mnew[g];
+        float ps = 0.f;
 #pragma unroll
-          for (int w2 = 0; w2 < NCW; ++w2) m2 = fmaxf(m2, wst[w2 * G + g]);
-          mnew[g] = m2;
-          f[g] = m_run[g] == -INFINITY ? 0.f : ex2(m_run[g] - m2);  // rescale of earlier sums
+        for (int pass = 0; pass < NPASS; ++pass) {
+          const float e = lg[pass] == -INFINITY ? 0.f : ex2(lg[pass] - mh);
+          ps += e;
+          if (row_writer) pw[(pass * RPW + rg) * G + myhead] = e;
         }
-        float sm[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) sm[g] = 0.f;
-        for (int r = t; r < nrows; r += 128)
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float e = ex2(slog[r * G + g] - mnew[g]);
-            slog[r * G + g] = e;
-            sm[g] += e;
-          }
+        for (int o = TPR; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+        if (head_writer) wxw[myhead] = ps;
+        __syncwarp();  // sums and probabilities visible to the whole warp
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) sm[g] += __shfl_xor_sync(0xffffffffu, sm[g], o);
-        }
-        named_bar(1, 128);  // every warp read the maxima before wst is reused for sums
-        if (lane == 0)
-#pragma unroll
-          for (int g = 0; g < G; ++g) wst[cw * G + g] = sm[g];
-        named_bar(1, 128);  // sums and probabilities visible to all compute warps
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float l2 = 0.f;
-#pragma unroll
-          for (int w2 = 0; w2 < NCW; ++w2) l2 += wst[w2 * G + g];
-          l_run[g] = l_run[g] * f[g] + l2;
+          l_run[g] = l_run[g] * f[g] + wxw[g];
           m_run[g] = mnew[g];
           const unsigned long long ff = pk(f[g], f[g]);
 #pragma unroll
@@ -403,24 +405,21 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
           }
         }
       }
-      // ---- V phase: o[g] += p[row][g] * v[row], lanes over the head dim ----
-      for (int i = 0; i < ntiles; ++i) {
-        const int j = it + ntiles + i, st = j % NST;
-        const bool got = __all_sync(0xffffffffu, ok && ab.wait(bar + 8 * st, (j / NST) & 1));
+      // ---------------- V half: o[g] += p[row][g] * v[row] ----------------
+      {
+        const int st = (it + 1) % NST;
+        const bool got = __all_sync(0xffffffffu, ok && ab.wait(bar + 8 * st, ((it + 1) / NST) & 1));
         ok = got;
         uint8_t *tile = smem + Gm::OFF_RING + st * Gm::TB;
-        const int arr = arow_local - i * ROWS;
-        const bool patched = sg.arow >= 0 && arr >= 0 && arr < ROWS;
         if (patched) {
           if (got) patch_row<D>(tile, p.v_new + (size_t)u * D, arr, t);
           named_bar(1, 128);
         }
         if (got) {
-          const int rmax = min(16, nrows - i * ROWS - cw * 16);  // this warp's rows in the tile
 #pragma unroll 4
-          for (int i2 = 0; i2 < 16; ++i2) {
-            if (i2 >= rmax) break;
-            const int rr = cw * 16 + i2;
+          for (int i2 = 0; i2 < WROWS; ++i2) {
+            if (i2 >= wrows) break;
+            const int rr = cw * WROWS + i2;
             unsigned long long v01, v23 = 0ull;
             if (D == 128) {
               const int chunk = lane >> 1, kb = chunk >> 3, ci = chunk & 7;
@@ -434,7 +433,7 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
                   tile + rr * 128 + ((ci ^ (rr & 7)) << 4) + (lane & 3) * 4);
               v01 = bf2(w);
             }
-            const float *pr = slog + (i * ROWS + rr) * G;
+            const float *pr = pw + i2 * G;
             float pv[G];
             if (G >= 4) {
 #pragma unroll
@@ -460,32 +459,57 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
           __syncwarp();
           if (lane == 0) mbar_arrive(bar + 32 + 8 * st);
         }
+        __syncwarp();  // pw and wxw are rewritten by the next tile
       }
-      it += 2 * ntiles;
-      named_bar(1, 128);  // slog and wst of this sub-chunk are done with
     }
-    // ---- merge the four warps' sums of this segment ----
+    // ---- merge the four warps' (max, normaliser, o) of this segment ----
+    if (lane == 0)
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+      for (int g = 0; g < G; ++g) wst[cw * G + g] = make_float2(m_run[g], l_run[g]);
+    named_bar(1, 128);
+    float Mg[G], Lg[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w2 = 0; w2 < NCW; ++w2) M = fmaxf(M, wst[w2 * G + g].x);
+      float L = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w2 = 0; w2 < NCW; ++w2) {
+          const float2 ml = wst[w2 * G + g];
+          if (ml.x != -INFINITY) L += ml.y * ex2(ml.x - M);
+        }
+      }
+      Mg[g] = M;
+      Lg[g] = L;
+      const float fw = m_run[g] == -INFINITY ? 0.f : ex2(m_run[g] - M);
 #pragma unroll
       for (int d = 0; d < DV / 2; ++d) {
         const float2 v = upk(o2[g][d]);
-        red[(cw * G + g) * D + lane * DV + 2 * d] = v.x;
-        red[(cw * G + g) * D + lane * DV + 2 * d + 1] = v.y;
+        atomicAdd(&red[g * D + lane * DV + 2 * d], v.x * fw);
+        atomicAdd(&red[g * D + lane * DV + 2 * d + 1], v.y * fw);
       }
+    }
     named_bar(1, 128);
     const bool direct = sg.nseg == 1;
     for (int e = t; e < G * D; e += 128) {
       const int g = e / D, d = e - g * D;
-      float O = 0.f;
+      float M = Mg[0], L = Lg[0];
 #pragma unroll
-      for (int w2 = 0; w2 < NCW; ++w2) O += red[(w2 * G + g) * D + d];
+      for (int h = 1; h < G; ++h)
+        if (g == h) {
+          M = Mg[h];
+          L = Lg[h];
+        }
+      const float O = red[e];
+      red[e] = 0.f;  // ready for the next segment (only this thread touches element e here)
       if (direct) {
-        p.out[(size_t)u * G * D + e] = __float2bfloat16(l_run[g] > 0.f ? O / l_run[g] : 0.f);
+        p.out[(size_t)u * G * D + e] = __float2bfloat16(L > 0.f ? O / L : 0.f);
         if (e < D / 8 && sg.arow >= 0) append_row<D>(p, u, sg.arow, sg.n_old, e);
       } else {
         p.part_o[(((size_t)u * T + sg.iseg) * G + g) * D + d] = O;
-        if (d == 0) p.part_ml[((size_t)u * T + sg.iseg) * G + g] = make_float2(m_run[g], l_run[g]);
+        if (d == 0) p.part_ml[((size_t)u * T + sg.iseg) * G + g] = make_float2(M, L);
       }
     }
     if (!direct) {
