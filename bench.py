@@ -62,6 +62,25 @@ def decode_bytes(n):
     return LY * B * (4 * HKV * n * D + 4 * HQ * D + 4 * HKV * D)
 
 
+def decode_traffic(rows_per_launch_avg):
+    """dram read + write bytes of one decode launch from the committed ncu capture, scaled
+    by the rows attended (traffic grows with them); None if the kernel sources changed
+    since the capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_kernel_traffic.json")) as f:
+            j = json.load(f)
+        h = hashlib.sha256()
+        for name in ("decode.cu", "kvc_internal.cuh"):
+            with open(os.path.join(ROOT, "attention_score_kv_snapkv_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != j["sources_sha256"] or j["units"] != UNITS:
+            return None
+        return (j["dram_read_bytes"] + j["dram_write_bytes"]) * rows_per_launch_avg / j["rows_per_unit"]
+    except Exception:
+        return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -392,6 +411,60 @@ def measure_stream(kvc, WL, dev, hbm_peak, steps=256):
             "steps_timed": steps, "launches_per_step": 2, "device_status": status}
 
 
+def run_profile_driver(args):
+    """Short fixed workloads for ncu captures (no timing printed):
+    decode: four launches of the 32-layer Mistral-shaped decode at n = 1100 on the
+            compact caches (the prompt is freed before the launches);
+    aux:    two layers of the H2O (OPT-6.7B) shape, prefill + 4 steps, then two layers
+            of the StreamingLLM (Llama-2-13B) shape, fill + 4 steady-state steps."""
+    import torch
+
+    import attention_score_kv_snapkv_gb300 as kvc
+    import workloads as WL
+
+    dev = torch.device("cuda")
+    if args.profile == "decode":
+        w = WL.MISTRAL
+        x = WL.snapkv_prompt(w, 5, dev)
+        res = kvc.snapkv_compress(x["Q_win"], x["K"], x["V"], keep_window=W, pool_kernel=P,
+                                  budget=KB, cap=KB + 256)
+        del x
+        torch.cuda.empty_cache()
+        q, _, _ = WL.decode_token(w, 0, 5, dev)
+        out = torch.empty_like(q)
+        for _ in range(4):
+            kvc.compressed_decode_attn(q, res["k"], res["v"], n_uniform=1100, out=out)
+    else:
+        w = WL.H2O_OPT
+        Ly = 2
+        st = kvc.H2OState(Ly, w.batch, w.kv_heads, w.head_dim, w.n_heavy, w.n_recent, dev)
+        for l in range(Ly):
+            Q, K, V = WL.h2o_prompt_layer(w, l, WL.seed_of(4), dev)
+            kvc.h2o_prefill(Q[None], K[None], V[None], n_heavy=w.n_heavy, n_recent=w.n_recent,
+                            state=st.layer(l))
+            del Q, K, V
+        for s in range(4):
+            q, kn, vn = WL.decode_token(w, s, WL.seed_of(4, 100), dev, layers=Ly)
+            kvc.h2o_decode_step(q, kn, vn, st, w.prompt_len + s)
+        torch.cuda.synchronize()
+        del st
+        torch.cuda.empty_cache()
+        w = WL.STREAM
+        S, R = w.n_sink, w.ring
+        kc = torch.zeros((Ly, w.batch, w.kv_heads, S + R, w.head_dim), dtype=torch.bfloat16, device=dev)
+        vc = torch.zeros_like(kc)
+        for t in range(S + R + 4):
+            q, k, v = WL.stream_token(w, t, WL.seed_of(5), dev, layers=Ly)
+            kvc.sink_window_append(k, v, kc, vc, t, n_sink=S, n_recent=R)
+            if t >= S + R:
+                kvc.compressed_decode_attn(q, kc, vc, n_uniform=S + R)
+    torch.cuda.synchronize()
+    status = kvc.kvc_device_status()
+    if status:
+        raise RuntimeError("device status flags %#x" % status)
+    return 0
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -570,7 +643,10 @@ def run_ours(args):
                         "eager_ms_per_token_all_layers": eager_ms_per_token},
         "roofline": {"kernel": "decode_kernel (compressed_decode_attn, %d layers per launch)" % LY,
                      "bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": dec_gbs / hbm_peak, "traffic": None,
+                     "frac": dec_gbs / hbm_peak,
+                     "traffic": decode_traffic(sum(KB + s + 1 for s in range(STEPS)) / STEPS),
+                     "traffic_source": "profiles/decode_kernel_traffic.json (ncu dram bytes of "
+                                       "one 32-layer launch at n = 1100, scaled by rows)",
                      "peak_kind": peak_kind + " burst copy"},
         "roofline_compress": {"kernel": "snapkv_compress (window vote + pool/top-k + gather)",
                               "bound": "hbm", "achieved": compress_bytes() / (comp_avg / 1e3) / 1e9,
@@ -609,6 +685,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-aux", action="store_true",
                     help="skip the long-context, H2O and streaming measurements")
+    ap.add_argument("--profile", choices=["decode", "aux"], default=None,
+                    help="run a short fixed workload for an ncu capture instead of the bench")
     ap.add_argument("--layers", type=int, default=32, help="profiling only: fewer layers")
     ap.add_argument("--decode-steps", type=int, default=256, help="profiling only")
     args = ap.parse_args()
@@ -619,6 +697,8 @@ def main():
         for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
             os.environ[v] = "1"  # the oracle runs on one core (set before numpy loads)
         return run_reference(args)
+    if args.profile:
+        return run_profile_driver(args)
     return run_ours(args)
 
 
