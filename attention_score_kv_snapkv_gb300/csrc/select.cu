@@ -168,21 +168,35 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
     if (d == 0) {
       // the top digit (sign and high exponent bits) puts most keys into a few bins:
       // one atomic per distinct bin of the warp
-      for (int j0 = warp * 32; j0 < n; j0 += NT) {
-        const int j = j0 + lane;
-        const uint32_t key = j < n ? kb[kidx(j)] : 0u;
-        const uint32_t vm = __ballot_sync(0xffffffffu, j < n);
-        if (j < n) {
-          const uint32_t bin = key >> sh;
-          const uint32_t grp = __match_any_sync(vm, bin);
-          if (lane == __ffs(grp) - 1) atomicAdd(&whist[bin], (uint32_t)__popc(grp));
+      for (int j1 = warp * 32; j1 < n; j1 += 8 * NT) {  // eight keys in flight per thread
+        uint32_t key8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = j1 + e * NT + lane;
+          key8[e] = j < n ? kb[kidx(j)] : 0u;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = j1 + e * NT + lane;
+          const uint32_t vm = __ballot_sync(0xffffffffu, j < n);
+          if (j < n) {
+            const uint32_t bin = key8[e] >> sh;
+            const uint32_t grp = __match_any_sync(vm, bin);
+            if (lane == __ffs(grp) - 1) atomicAdd(&whist[bin], (uint32_t)__popc(grp));
+          }
         }
       }
     } else {
       // lower digits of the keys left in the bucket: spread bins, plain atomics
-      for (int j = warp * 32 + lane; j < n; j += NT) {
-        const uint32_t key = kb[kidx(j)];
-        if ((key & mask_hi) == prefix) atomicAdd(&whist[(key >> sh) & (NBIN - 1)], 1u);
+      // (eight keys in flight per thread: the keys may live in global memory)
+      for (int j1 = warp * 32 + lane; j1 < n; j1 += 8 * NT) {
+        uint32_t key8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) key8[e] = j1 + e * NT < n ? kb[kidx(j1 + e * NT)] : ~prefix;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (j1 + e * NT < n && (key8[e] & mask_hi) == prefix)
+            atomicAdd(&whist[(key8[e] >> sh) & (NBIN - 1)], 1u);
       }
     }
     __syncthreads();
@@ -264,11 +278,11 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
     int gt_before = gt_base + (excl & 0xffff), eq_before = eq_base + (excl >> 16);
     if (gt + eq > 0) {
       int out = gt_before + min(eq_before, need);
+#pragma unroll 8
       for (int i = 0; i < RUN; ++i) {
         const int j = j0 + i;
-        if (j >= n) break;
-        const uint32_t key = kb[kidx(j)];
-        const bool take = key > T || (key == T && eq_before++ < need);
+        const uint32_t key = j < n ? kb[kidx(j)] : 0u;
+        const bool take = j < n && (key > T || (key == T && eq_before++ < need));
         if (take) {
           if (out < p.k) sel[out] = j;
           ++out;
