@@ -7,12 +7,13 @@
 //   1. logits of the G query heads against every live row (the new token's row comes
 //      straight from k_new, so nothing waits on its write);
 //   2. exact softmax normaliser per head (block reduction);
-//   3. o = P.V with lanes over the head dim, merged over the 8 warps;
+//   3. o = P.V, merged over the 8 warps;
 //   4. score[e] += sum_g p_g[e] (the new entry starts from 0);
 //   5. if the unit now holds every slot: evict the smallest score among positions
 //      <= t - n_recent, the higher position on exact ties; its slot becomes free.
 // The step is HBM-bound: each live K and V row is read once (plus 12 bytes of score
-// and position per entry).
+// and position per entry).  Rows are read as 16-byte chunks, D/8 lanes per row, four
+// loads in flight per lane, so a CTA keeps about 16 KB of each phase's rows in flight.
 #include <math.h>
 
 #include "kvc_internal.cuh"
@@ -35,24 +36,8 @@ struct H2OP {
   uint32_t *status;
 };
 
-template <int D>
-__device__ __forceinline__ void load_row(const __nv_bfloat16 *row, int lane, float (&f)[D / 32]) {
-  if (D == 128) {
-    const uint2 w = *reinterpret_cast<const uint2 *>(row + 4 * lane);
-    f[0] = bf_lo(w.x);
-    f[1] = bf_hi(w.x);
-    f[2 % (D / 32)] = bf_lo(w.y);
-    f[3 % (D / 32)] = bf_hi(w.y);
-  } else {
-    const uint32_t w = *reinterpret_cast<const uint32_t *>(row + 2 * lane);
-    f[0] = bf_lo(w);
-    f[1 % (D / 32)] = bf_hi(w);
-  }
-}
-
 template <int D, int G>
 __global__ void __launch_bounds__(NT) h2o_step_kernel(const H2OP p) {
-  constexpr int DV = D / 32;
   extern __shared__ float hs[];
   float *qs = hs;                         // [G][D]
   float *lg = qs + G * D;                 // [G][slots]: logits, then probabilities
@@ -76,34 +61,40 @@ __global__ void __launch_bounds__(NT) h2o_step_kernel(const H2OP p) {
     qs[e] = __bfloat162float(p.q[(size_t)u * G * D + e]) * p.c;
   __syncthreads();
 
-  // 1. logits: warp per row, lanes over the head dim
-  float qreg[G][DV];
+  // 1. logits.  D/8 lanes per row, each with one 16-byte chunk (8 head dims), so a warp
+  // load covers 32/(D/8) rows; four such loads are in flight per lane before any is used.
+  constexpr int LPR = D / 8;     // lanes per row
+  constexpr int RPL = 32 / LPR;  // rows per warp load
+  constexpr int NB = 4;          // loads in flight per lane
+  const int sub = lane / LPR, ch = lane % LPR;
+  float qreg[G][8];
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int d = 0; d < DV; ++d) qreg[g][d] = qs[g * D + lane * DV + d];
-  for (int e0 = warp; e0 < count; e0 += 4 * NW) {
-    float kf[4][DV];
+    for (int d = 0; d < 8; ++d) qreg[g][d] = qs[g * D + ch * 8 + d];
+  for (int e0 = warp * RPL; e0 < count; e0 += NB * NW * RPL) {
+    uint4 kw[NB];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = e0 + i * NW;
+    for (int i = 0; i < NB; ++i) {
+      const int e = e0 + i * NW * RPL + sub;
       if (e < count) {
         const __nv_bfloat16 *src = (e == f) ? p.k_new + (size_t)u * D : p.k + (rowbase + e) * D;
-        load_row<D>(src, lane, kf[i]);
+        kw[i] = *reinterpret_cast<const uint4 *>(src + ch * 8);
       }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = e0 + i * NW;
-      if (e >= count) break;
+    for (int i = 0; i < NB; ++i) {
+      const int e = e0 + i * NW * RPL + sub;
+      const float kf[8] = {bf_lo(kw[i].x), bf_hi(kw[i].x), bf_lo(kw[i].y), bf_hi(kw[i].y),
+                           bf_lo(kw[i].z), bf_hi(kw[i].z), bf_lo(kw[i].w), bf_hi(kw[i].w)};
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float a = 0.f;
 #pragma unroll
-        for (int d = 0; d < DV; ++d) a = fmaf(qreg[g][d], kf[i][d], a);
+        for (int d = 0; d < 8; ++d) a = fmaf(qreg[g][d], kf[d], a);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-        if (lane == 0) lg[g * S + e] = a;
+        for (int o = LPR / 2; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (ch == 0 && e < count) lg[g * S + e] = a;
       }
     }
   }
@@ -152,38 +143,50 @@ __global__ void __launch_bounds__(NT) h2o_step_kernel(const H2OP p) {
   }
   __syncthreads();
 
-  // 3. o = P.V
-  float o[G][DV];
+  // 3. o = P.V with the same row layout (lane: one row, 8 head dims); the RPL rows of a
+  // warp load are summed by shuffles at the end
+  float o[G][8];
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int d = 0; d < DV; ++d) o[g][d] = 0.f;
-  for (int e0 = warp; e0 < count; e0 += 4 * NW) {
-    float vf[4][DV];
+    for (int d = 0; d < 8; ++d) o[g][d] = 0.f;
+  for (int e0 = warp * RPL; e0 < count; e0 += NB * NW * RPL) {
+    uint4 vw[NB];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = e0 + i * NW;
+    for (int i = 0; i < NB; ++i) {
+      const int e = e0 + i * NW * RPL + sub;
       if (e < count) {
         const __nv_bfloat16 *src = (e == f) ? p.v_new + (size_t)u * D : p.v + (rowbase + e) * D;
-        load_row<D>(src, lane, vf[i]);
+        vw[i] = *reinterpret_cast<const uint4 *>(src + ch * 8);
       }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = e0 + i * NW;
-      if (e >= count) break;
+    for (int i = 0; i < NB; ++i) {
+      const int e = e0 + i * NW * RPL + sub;
+      if (e < count) {
+        const float vf[8] = {bf_lo(vw[i].x), bf_hi(vw[i].x), bf_lo(vw[i].y), bf_hi(vw[i].y),
+                             bf_lo(vw[i].z), bf_hi(vw[i].z), bf_lo(vw[i].w), bf_hi(vw[i].w)};
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float pe = lg[g * S + e];
+        for (int g = 0; g < G; ++g) {
+          const float pe = lg[g * S + e];
 #pragma unroll
-        for (int d = 0; d < DV; ++d) o[g][d] = fmaf(pe, vf[i][d], o[g][d]);
+          for (int d = 0; d < 8; ++d) o[g][d] = fmaf(pe, vf[d], o[g][d]);
+        }
       }
     }
   }
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int d = 0; d < DV; ++d) red[(warp * G + g) * D + lane * DV + d] = o[g][d];
+    for (int d = 0; d < 8; ++d) {
+#pragma unroll
+      for (int o2 = LPR; o2 < 32; o2 <<= 1) o[g][d] += __shfl_xor_sync(0xffffffffu, o[g][d], o2);
+    }
+  if (sub == 0)
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int d = 0; d < 8; ++d) red[(warp * G + g) * D + ch * 8 + d] = o[g][d];
 
   // 4. scores; 5. eviction candidates (per-thread best, then block reduction)
   float best_s = INFINITY;
