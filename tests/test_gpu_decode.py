@@ -123,3 +123,49 @@ def test_rows_past_n_are_never_read_into_the_output(kvc):
     out = kvc.compressed_decode_attn(q.to(dev), kc2.to(dev), vc2.to(dev), n_valid=n.to(dev))
     assert torch.isfinite(out.float()).all()
     assert_outputs_close(f64(out), oracle_decode(q, kc, vc, n.numpy()))
+
+
+MANY_TILES = [  # Ly, B, Hq, Hkv, D, cap: units x tile slots well above the resident grid
+    (1, 16, 32, 8, 128, 2304),
+    (2, 8, 32, 4, 64, 2100),
+    (1, 24, 8, 8, 128, 1500),
+]
+
+
+@pytest.mark.parametrize("shape", MANY_TILES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("append", [False, True], ids=["attend", "append"])
+def test_decode_many_tiles_per_cta(kvc, shape, append):
+    """Each CTA streams several tiles of several units: the shared-memory ring wraps many
+    times, units split over CTAs merge through the workspace, and ragged row counts
+    (including empty units, empty segments and, with the append, a full unit) mix."""
+    Ly, B, Hq, Hkv, D, cap = shape
+    q, kc, vc = rand_cache(Ly, B, Hq, Hkv, D, cap, seed=cap + Hkv + (1 if append else 0))
+    g = torch.Generator().manual_seed(cap)
+    n0 = torch.randint(0, cap + 1, (Ly, B, Hkv), generator=g, dtype=torch.int32)
+    flat = n0.view(-1)
+    flat[0], flat[1], flat[2], flat[-1] = 0, cap, 1, cap - 1
+    flat[3:8] = torch.tensor([128, 129, 127, 0, 2 * 128])
+    dev = torch.device("cuda")
+    kcd, vcd, nd = kc.to(dev), vc.to(dev), n0.to(dev)
+    if append:
+        kn = torch.randn((Ly, B, Hkv, D), generator=g).to(torch.bfloat16)
+        vn = torch.randn((Ly, B, Hkv, D), generator=g).to(torch.bfloat16)
+        out = kvc.compressed_decode_attn(q.to(dev), kcd, vcd, n_valid=nd, k_new=kn.to(dev),
+                                         v_new=vn.to(dev))
+        torch.cuda.synchronize()
+        st = kvc.kvc_device_status()
+        assert st & kvc.DEV_CACHE_FULL and st & ~kvc.DEV_CACHE_FULL == 0, st
+        kc2, vc2, n1 = kc.clone(), vc.clone(), n0.clone()
+        for idx in np.ndindex(*n0.shape):
+            if int(n0[idx]) < cap:
+                kc2[idx + (int(n0[idx]),)] = kn[idx]
+                vc2[idx + (int(n0[idx]),)] = vn[idx]
+                n1[idx] += 1
+        assert torch.equal(nd.cpu(), n1)
+        assert torch.equal(kcd.cpu(), kc2) and torch.equal(vcd.cpu(), vc2)
+        assert_outputs_close(f64(out), oracle_decode(q, kc2, vc2, n1.numpy()))
+    else:
+        out = kvc.compressed_decode_attn(q.to(dev), kcd, vcd, n_valid=nd)
+        torch.cuda.synchronize()
+        assert kvc.kvc_device_status() == 0
+        assert_outputs_close(f64(out), oracle_decode(q, kc, vc, n0.numpy()))
