@@ -7,32 +7,41 @@
 // unit's finishing CTA writes it to the cache, its position and the new n_valid).
 //
 // Design (sm_103a, HBM-bound: every cached K/V byte is read once):
-// * persistent stream-K: all units' 64-row tile slots form one sequence that is split
-//   evenly over a grid of resident CTAs (three per SM), so every CTA streams the same
-//   number of tiles; a CTA's range covers segments of one or more units.  Warp 0
-//   streams each segment's tiles as K0, V0, K1, V1, ... through one continuous 4-stage
-//   shared-memory ring with TMA (128-byte swizzle, one mbarrier pair per stage), so the
-//   next segment's loads overlap the current segment's epilogue; warps 1-4 compute.
-//   The throughput of a CTA is the bytes in flight over the memory latency, so the
-//   shared memory goes to the ring: no logit buffer, no block-wide softmax.
-// * each compute warp owns 16 rows of every tile, in both halves of the step, and keeps
-//   its own online softmax (running max, normaliser and o per head; FlashAttention's
-//   rescaling), so a tile needs no synchronisation between the warps.
-// * K half: D/8 threads per row, each owning one 16-byte chunk (8 head dims) of the row
-//   (conflict-free reads of the swizzled tile); the thread's slice of q, pre-scaled by
-//   log2(e)/sqrt(D), lives in registers (a bulk copy brings each unit's q to shared
-//   memory ahead of time); packed fp32x2 FMA; a transpose-reduce over the row's lanes
-//   leaves one head's logit per lane.  The warp's 16 probabilities per head go through
-//   a small per-warp buffer to every lane.
-// * V half: lanes over the head dim, packed FMA with those probabilities.  Rows at or
-//   past n are never touched.
-// * at the end of a segment the four warps' (max, normaliser, o) merge in shared
-//   memory; a unit covered by one segment is written directly, otherwise each
-//   segment's (max, normaliser, o) goes to the workspace and the last CTA to finish one
-//   of the unit's segments (atomic counter, no waiting) merges them and writes the bf16
-//   output, resetting the counter.  The counters live in a fixed 256 KB header of the
-//   workspace (one int per unit, at most 65535 units) that is zero between calls,
-//   whatever the call shapes.
+// * persistent stream-K: all units' 128-row tile slots form one sequence that is split
+//   evenly over one resident CTA per SM, so every CTA streams the same number of tiles;
+//   a CTA's range covers segments of one or more units.  It works on its last unit
+//   first (usually shared with the next CTA), then the others in order, so units split
+//   between two CTAs are finished early by both and the tail of the kernel is a whole
+//   unit without a merge.  Before waiting for the previous kernel (programmatic
+//   dependent launch) the CTA prefetches its first tiles into L2.
+// * warp 0 streams each segment's tiles as K0, V0, K1, V1, ... through a 4-stage
+//   shared-memory ring with TMA (128-byte swizzle), so K tiles always use the even
+//   stages and V tiles the odd ones.  The producer writes the tile index into a per-stage
+//   tag before each load and the MMA issuer waits for its tag before it trusts the
+//   stage's full-barrier parity.
+// * the logits run on the tensor cores: warp 1 issues S^T = K_tile . q^T with
+//   tcgen05.mma (M = 128 key rows, N = 16 columns holding the G query heads, K = D;
+//   bf16 in, fp32 accumulator in TMEM, two buffers of 16 columns); the K stage and the
+//   unit's q buffer are released by the MMA's own commits.  The compute warps write q
+//   into rows 0..G-1 of a 16-row operand (double-buffered, 128-byte swizzle) whose other
+//   rows stay zero.
+// * warps 2-9 (two per TMEM lane quarter) read each key's G logits from TMEM (one lane
+//   per key) and keep an online softmax (FlashAttention's rescaling): one warp-wide max
+//   per head and tile (redux.sync), per-lane normalisers summed only at the end of the
+//   segment, and o rescaled only when a max grew.  V half: lanes over the head dim,
+//   each warp over its 16 rows of the tile, packed fp32x2 FMA with the probabilities
+//   passed as (p, p) pairs through a small per-warp buffer.  Rows at or past n are
+//   never touched.
+// * at the end of a segment each compute warp stages its (max, normaliser, o) in shared
+//   memory (double-buffered) and moves on; warps 10-13 merge the eight warps' states.
+//   A unit covered by one segment is written directly; otherwise each segment's (max,
+//   normaliser, o) goes to the workspace and the last CTA to finish one of the unit's
+//   segments (atomic counter, no waiting) merges them and writes the bf16 output,
+//   resetting the counter.  The counters live in a fixed 256 KB header of the workspace
+//   (one int per unit, at most 65535 units) that is zero between calls, whatever the
+//   call shapes.
+// * every wait is bounded (on expiry the CTA sets the device timeout flag and abandons
+//   its work), and the V reader checks the stage tag as a self-check of the ring.
 #include <math.h>
 
 #include "kvc_internal.cuh"
@@ -40,32 +49,76 @@
 namespace kvc {
 namespace {
 
-constexpr int ROWS = 64;     // rows per tile
-constexpr int NST = 4;       // ring depth (K or V tiles)
-constexpr int NCW = 4;       // compute warps
-constexpr int WROWS = ROWS / NCW;  // rows of a tile per compute warp
-constexpr int NTH = 32 * (NCW + 1);
+constexpr int ROWS = 128;    // rows per tile (the MMA's M)
+constexpr int NST = 4;         // ring depth (K or V tiles; K in even stages, V in odd)
+constexpr int NCW = 8;         // compute warps: NCW / 4 per TMEM lane quarter
+constexpr int WROWS = ROWS / NCW;  // rows of a tile per compute warp in the V half
+constexpr int NEW = 4;         // epilogue warps: merge each segment's warp states
+constexpr int NTH = 32 * (NCW + NEW + 2);
+constexpr int EPI0 = 32 * (NCW + 2);  // first epilogue thread
+constexpr int MINB = 1;        // resident CTAs per SM
+static_assert(NCW % 4 == 0 && WROWS <= 32 && NST <= 8 && NST % 2 == 0, "geometry");
+constexpr int QN = 16;       // MMA N: query heads padded with zero rows
+constexpr int TMEM_COLS = 32;  // two 16-column S^T buffers
 
 template <int D, int G>
 struct DGeo {
   static constexpr int KB = D / 64;
   static constexpr int KBLK = ROWS * 128;        // bytes of one k-block of a tile
   static constexpr int TB = KB * KBLK;           // bytes of one K or V tile
-  static constexpr int QB = G * D * 2;           // bytes of one unit's q (bf16)
+  static constexpr int QBLK = QN * 128;          // bytes of one k-block of the q operand
+  static constexpr int QOP = KB * QBLK;          // bytes of one q operand
   static constexpr int OFF_RING = 0;
-  static constexpr int OFF_QB = NST * TB;                    // bf16 [2][G][D]
-  static constexpr int OFF_P = OFF_QB + 2 * QB;              // fp32 [NCW][WROWS][G] probabilities
-  static constexpr int OFF_RED = OFF_P + NCW * WROWS * G * 4;  // fp32 [G][D] merged o
-  static constexpr int OFF_WX = OFF_RED + G * D * 4;         // fp32 [NCW][G] tile max / sum
-  static constexpr int OFF_ST = OFF_WX + NCW * G * 4;        // float2 [NCW][G] (max, normaliser)
-  static constexpr int OFF_BAR = OFF_ST + NCW * G * 8;
-  static constexpr int SMEM = OFF_BAR + 128 + 1024;
+  static constexpr int OFF_Q = NST * TB;                     // [2] q operands (1024-aligned)
+  static constexpr int OFF_P = OFF_Q + 2 * QOP;              // (p, p) pairs [NCW][WROWS][G]
+  static constexpr int OFF_STAGE = OFF_P + NCW * WROWS * G * 8;  // fp32 [2][NCW][G][D] warp o
+  static constexpr int OFF_SST = OFF_STAGE + 2 * NCW * G * D * 4;  // float2 [2][NCW][G] (m, l)
+  static constexpr int OFF_SCL = OFF_SST + 2 * NCW * G * 8;  // fp32 [NCW][G] warp weights
+  static constexpr int OFF_ML = OFF_SCL + NCW * G * 4;       // float2 [G] segment (M, L)
+  static constexpr int OFF_BAR = OFF_ML + G * 8;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;
   static constexpr int DV = D / 32;              // head-dim elements per lane in the V half
-  static constexpr int TPR = D / 8;              // K half: threads per row, one chunk each
-  static constexpr int RPW = 32 / TPR;           // K half: rows per warp and pass
-  static constexpr int NPASS = WROWS / RPW;      // K half: passes over the warp's rows
-  static_assert(G <= TPR, "every head's logit needs a lane of the row");
+  static_assert(G <= QN, "the query heads must fit the MMA's N");
+  static_assert(QOP % 1024 == 0 && TB % 1024 == 0, "swizzled operands stay 1024-aligned");
 };
+
+// barrier offsets (bytes from OFF_BAR)
+constexpr int B_FULL = 0;      // [NST] ring stage filled (TMA)
+constexpr int B_EMPTY = 64;    // [NST] ring stage free (MMA commit for K, NCW warps for V)
+constexpr int B_QFULL = 128;   // [2] q operand written (NCW compute warps)
+constexpr int B_QEMPTY = 144;  // [2] q operand no longer read (MMA commit after the unit)
+constexpr int B_SFULL = 160;   // [2] S^T buffer written (MMA commit)
+constexpr int B_SEMPTY = 176;  // [2] S^T buffer read (NCW warps)
+constexpr int B_RFULL = 192;   // [2] segment warp states staged (NCW compute warps)
+constexpr int B_REMPTY = 208;  // [2] staged states consumed (epilogue)
+constexpr int B_ABORT = 224;   // int
+constexpr int B_LAST = 228;    // int
+constexpr int B_TMEM = 232;    // uint32
+constexpr int B_EOK = 236;     // int: the epilogue's wait succeeded
+constexpr int B_TAG = 256;     // int [NST]: the tile index last issued into each stage
+static_assert(B_TAG + 4 * NST <= 512, "barrier area");
+
+// L2 prefetch of one box of a 2-D tensor map (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap *map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
+}
+
+// Bounded spin until a stage's tile tag reaches `want` (it is written by the producer
+// after the stage was released and before its load is issued, so once it matches, the
+// stage's full barrier is at most one phase from the awaited one).
+__device__ __forceinline__ bool wait_tag(volatile int *tag, int want, const Abort &ab) {
+  if (*tag == want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 26); ++it) {
+    if (*tag == want) return true;
+    if (ab.raised()) return false;
+    if ((it & 15u) == 0 && globaltimer_ns() - t0 > ab.limit) break;
+    __nanosleep(32);
+  }
+  ab.raise();
+  return false;
+}
 
 struct DecP {
   const __nv_bfloat16 *q;
@@ -76,7 +129,7 @@ struct DecP {
   int32_t *pos;            // [U, cap] or null
   int new_pos;
   int n_uniform, cap;
-  int units, tiles_per_unit;  // tile slots of 64 rows per unit (for n <= cap)
+  int units, tiles_per_unit;  // tile slots of ROWS rows per unit (for n <= cap)
   __nv_bfloat16 *out;
   float2 *part_ml;         // [U][T][G] per-segment (max, normaliser)
   float *part_o;           // [U][T][G][D] per-segment unnormalised o
@@ -161,8 +214,9 @@ __device__ __forceinline__ Seg seg_geo(const DecP &p, int u, int b, int s0, int 
 }
 
 
+
 template <int D, int G>
-__global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ CUtensorMap tk,
+__global__ void __launch_bounds__(NTH, MINB) decode_kernel(const __grid_constant__ CUtensorMap tk,
                                                      const __grid_constant__ CUtensorMap tv,
                                                      const DecP p) {
   using Gm = DGeo<D, G>;
@@ -170,13 +224,11 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
-  float *red = reinterpret_cast<float *>(smem + Gm::OFF_RED);   // [G][D] merged o
-  float *wx = reinterpret_cast<float *>(smem + Gm::OFF_WX);     // [NCW][G] tile max / sum
-  float2 *wst = reinterpret_cast<float2 *>(smem + Gm::OFF_ST);  // [NCW][G] (max, normaliser)
-  // barriers: full[NST] at +0, empty[NST] at +32, qfull[2] at +64, qempty[2] at +80
   const uint32_t bar = sb + Gm::OFF_BAR;
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Gm::OFF_BAR + 96);
-  volatile int *last_flag = reinterpret_cast<volatile int *>(smem + Gm::OFF_BAR + 100);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Gm::OFF_BAR + B_ABORT);
+  volatile int *last_flag = reinterpret_cast<volatile int *>(smem + Gm::OFF_BAR + B_LAST);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Gm::OFF_BAR + B_TMEM);
+  volatile int *tag = reinterpret_cast<volatile int *>(smem + Gm::OFF_BAR + B_TAG);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Abort ab{abort_flag, p.status, p.timeout};
@@ -184,26 +236,59 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
   const int total = p.units * T, Q = total / P, R = total % P;
   const int s0 = slot_first(b, Q, R), s1 = slot_first(b + 1, Q, R);
   const int u_first = s0 / T, u_last = s1 > s0 ? (s1 - 1) / T : u_first - 1;
+  // Order of the CTA's units: its last unit (usually shared with the next CTA) first,
+  // then the others in order.  Every unit shared with a neighbour is then worked on
+  // early by both CTAs, so the split merges happen early and a CTA's final segment is
+  // usually a whole unit, written without the merge.
+  const int nu = u_last - u_first + 1;
+  auto unit_at = [&](int kk) { return kk == 0 ? u_last : u_first + kk - 1; };
 
-  for (int e = threadIdx.x; e < G * D; e += NTH) red[e] = 0.f;
+  // both q operands start zero: TMA later writes only their rows 0..G-1
+  for (int e = threadIdx.x; e < 2 * Gm::QOP / 16; e += NTH)
+    reinterpret_cast<uint4 *>(smem + Gm::OFF_Q)[e] = make_uint4(0, 0, 0, 0);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // seen by the tensor cores
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int i = 0; i < NST; ++i) {
-      mbar_init(bar + 8 * i, 1);
-      mbar_init(bar + 32 + 8 * i, NCW);
+      tag[i] = -1;
+      mbar_init(bar + B_FULL + 8 * i, 1);
+      mbar_init(bar + B_EMPTY + 8 * i, NCW);  // V: 8 warps; K: 8 commits of its MMA
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar + 64 + 8 * i, 1);
-      mbar_init(bar + 80 + 8 * i, NCW);
+      mbar_init(bar + B_QFULL + 8 * i, NCW);  // the compute warps wrote the unit's q
+      mbar_init(bar + B_QEMPTY + 8 * i, 1);   // the MMAs of the unit have completed
+      mbar_init(bar + B_SFULL + 8 * i, 1);
+      mbar_init(bar + B_SEMPTY + 8 * i, NCW);
+      mbar_init(bar + B_RFULL + 8 * i, NCW);
+      mbar_init(bar + B_REMPTY + 8 * i, 1);
     }
     fence_mbar_init();
   }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
   // Programmatic dependent launch: the next kernel of the stream may start launching
   // now (its CTAs take SM slots as this grid's CTAs exit, and wait here until this grid
   // has completed); this grid waits for the previous kernel before reading anything
   // it wrote (q, the caches, n_valid, the workspace counters).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0 && nu > 0) {
+    // While the previous kernel finishes: pull the first tiles of this CTA's first unit
+    // into L2 (slot range only; the row count is not read before the wait).  L2 stays
+    // coherent with that kernel's writes, so this is only a hint.
+    const int u = unit_at(0);
+    const int t_lo = max(s0, u * T) - u * T, t_hi = min(s1, (u + 1) * T) - u * T;
+    for (int t2 = t_lo; t2 < t_hi && t2 < t_lo + NST / 2; ++t2)
+      for (int kb = 0; kb < Gm::KB; ++kb) {
+        tma_prefetch_l2(&tk, kb * 64, u * p.cap + t2 * ROWS);
+        tma_prefetch_l2(&tv, kb * 64, u * p.cap + t2 * ROWS);
+      }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
@@ -213,339 +298,389 @@ __global__ void __launch_bounds__(NTH, 3) decode_kernel(const __grid_constant__ 
       tma_prefetch_desc(&tv);
       int it = 0, k = 0;
       bool ok = true;
-      for (int u = u_first; u <= u_last && ok; ++u, ++k) {
+      for (; k < nu && ok; ++k) {
+        const int u = unit_at(k);
         const Seg g = seg_geo(p, u, b, s0, s1, T, Q, R, false);
-        const int qb = k & 1;
-        if (!ab.wait(bar + 80 + 8 * qb, ((k >> 1) & 1) ^ 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar + 64 + 8 * qb, Gm::QB);
-        bulk_load(sb + Gm::OFF_QB + qb * Gm::QB, p.q + (size_t)u * G * D, Gm::QB, bar + 64 + 8 * qb);
         const int ntiles = (g.r1 - g.r0 + ROWS - 1) / ROWS;
         for (int i = 0; i < 2 * ntiles; ++i, ++it) {
           const int st = it % NST, use = it / NST;
-          if (!ab.wait(bar + 32 + 8 * st, (use & 1) ^ 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar + 8 * st, Gm::TB);
+          if (!ab.wait(bar + B_EMPTY + 8 * st, (use & 1) ^ 1)) { ok = false; break; }
+          __threadfence_block();  // the release seen above comes before the new tag
+          tag[st] = it;
+          mbar_arrive_expect_tx(bar + B_FULL + 8 * st, Gm::TB);
           const int row = u * p.cap + g.r0 + (i >> 1) * ROWS;
           const CUtensorMap *map = (i & 1) ? &tv : &tk;
           for (int kb = 0; kb < Gm::KB; ++kb)
             tma_load_2d(sb + Gm::OFF_RING + st * Gm::TB + kb * Gm::KBLK, map, kb * 64, row,
-                        bar + 8 * st);
+                        bar + B_FULL + 8 * st);
         }
       }
       for (int st = 0; st < NST; ++st) {  // drain
         const int cnt = it / NST + (st < it % NST ? 1 : 0);
-        if (cnt > 0) mbar_wait_bounded(bar + 8 * st, (cnt - 1) & 1, p.timeout);
+        if (cnt > 0) mbar_wait_bounded(bar + B_FULL + 8 * st, (cnt - 1) & 1, p.timeout);
       }
-      for (int qb = 0; qb < 2; ++qb) {
-        const int cnt = k / 2 + (qb < k % 2 ? 1 : 0);
-        if (cnt > 0) mbar_wait_bounded(bar + 64 + 8 * qb, (cnt - 1) & 1, p.timeout);
-      }
+      (void)k;
     }
-    return;
-  }
-
-  // ------------------------------ compute warps ------------------------------
-  const int cw = warp - 1;         // 0..3: owns rows [cw*WROWS, (cw+1)*WROWS) of every tile
-  const int t = threadIdx.x - 32;  // 0..127
-  constexpr int TPR = Gm::TPR, RPW = Gm::RPW, NPASS = Gm::NPASS, DV = Gm::DV;
-  constexpr int WMASK = TPR / G - 1;  // lanes of a row holding the same head's logit
-  const int rg = lane / TPR;          // K half: row within the warp's pass
-  const int sl = lane % TPR;          // K half: the thread's 16-byte chunk of the row
-  // the head whose logit this lane holds after the transpose-reduce (see below)
-  int myhead = 0;
+  } else if (warp == 1) {
+    // ---------- MMA issuer: S^T = K_tile . q^T for every K tile, into TMEM ----------
+    if (lane == 0) {
+      int it = 0, k = 0, sc = 0, last_sb = -1, last_par = 0;
+      bool ok = true;
+      const uint32_t idesc = idesc_bf16(ROWS, QN);
+      for (; k < nu && ok; ++k) {
+        const int u = unit_at(k);
+        const Seg g = seg_geo(p, u, b, s0, s1, T, Q, R, false);
+        const int qb = k & 1;
+        if (!ab.wait(bar + B_QFULL + 8 * qb, (k >> 1) & 1)) { ok = false; break; }
+        const uint64_t qd = sdesc_k128(sb + Gm::OFF_Q + qb * Gm::QOP);
+        const int ntiles = (g.r1 - g.r0 + ROWS - 1) / ROWS;
+        const int arow_local = g.arow - g.r0;
+        for (int i = 0; i < ntiles; ++i, ++sc) {
+          const int j = it + 2 * i, st = j % NST;
+          const int sbf = sc & 1;
+          // wait until the producer has reissued the stage before trusting the full
+          // barrier's parity (needed whenever a stage's previous use was released by
+          // other warps, as with an odd ring depth; cheap otherwise)
+          if (!wait_tag(tag + st, j, ab)) { ok = false; break; }
+          __threadfence_block();
+          if (!ab.wait(bar + B_FULL + 8 * st, (j / NST) & 1)) { ok = false; break; }
+          if (!ab.wait(bar + B_SEMPTY + 8 * sbf, ((sc >> 1) & 1) ^ 1)) { ok = false; break; }
+          const int arr = arow_local - i * ROWS;
+          if (g.arow >= 0 && arr >= 0 && arr < ROWS) {  // the appended row, from k_new
+            uint8_t *tile = smem + Gm::OFF_RING + st * Gm::TB;
+            for (int c = 0; c < D / 8; ++c) patch_row<D>(tile, p.k_new + (size_t)u * D, arr, c);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          }
+          tc_fence_after();
+          const uint64_t kd = sdesc_k128(sb + Gm::OFF_RING + st * Gm::TB);
+          const uint32_t d = tmem + (uint32_t)(sbf * QN);
 #pragma unroll
-  for (int lvl = TPR / 2, nv = G; lvl >= 1; lvl >>= 1)
-    if (nv >= 2) {
-      if (lane & lvl) myhead += nv / 2;
-      nv /= 2;
+          for (int kb = 0; kb < Gm::KB; ++kb) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ko = (uint64_t)((kb * Gm::KBLK + kk * 32) >> 4);
+              const uint64_t qo = (uint64_t)((kb * Gm::QBLK + kk * 32) >> 4);
+              umma_bf16(d, kd + ko, qd + qo, idesc, (kb | kk) != 0);
+            }
+          }
+          umma_commit(bar + B_SFULL + 8 * sbf);
+          // the K stage is free once these MMAs complete: one commit plus NCW - 1 plain
+          // arrivals, so the stage's NCW-count barrier completes on the commit
+          umma_commit(bar + B_EMPTY + 8 * st);
+#pragma unroll
+          for (int r = 1; r < NCW; ++r) mbar_arrive(bar + B_EMPTY + 8 * st);
+          last_sb = sbf;
+          last_par = (sc >> 1) & 1;
+        }
+        if (!ok) break;
+        it += 2 * ntiles;
+        umma_commit(bar + B_QEMPTY + 8 * qb);  // q buffer free once this unit's MMAs complete
+      }
+      // drain: every commit issued has arrived before the CTA may exit (commits complete
+      // in order, so the last one covers the rest)
+      if (ok && k > 0) mbar_wait_bounded(bar + B_QEMPTY + 8 * ((k - 1) & 1), ((k - 1) >> 1) & 1, p.timeout);
+      else if (last_sb >= 0) mbar_wait_bounded(bar + B_SFULL + 8 * last_sb, last_par, p.timeout);
     }
-  const bool row_writer = (lane & WMASK) == 0;        // one lane per (row, head)
-  const bool head_writer = row_writer && lane < TPR;  // one lane per head
-  float *pw = reinterpret_cast<float *>(smem + Gm::OFF_P) + cw * WROWS * G;  // [WROWS][G]
-  float *wxw = wx + cw * G;
-  int it = 0, k = 0;
-  bool ok = true;
-  for (int u = u_first; u <= u_last; ++u, ++k) {
-    const Seg sg = seg_geo(p, u, b, s0, s1, T, Q, R, t == 0);
-    // q slice of this thread: chunk sl of every head, fp32 pairs, pre-scaled
-    unsigned long long qr[G][4];
-    {
-      const int qb = k & 1;
-      const bool got = __all_sync(0xffffffffu, ok && ab.wait(bar + 64 + 8 * qb, (k >> 1) & 1));
-      ok = got;
-      const uint8_t *qsm = smem + Gm::OFF_QB + qb * Gm::QB;
+  } else if (warp < 2 + NCW) {
+    // ------------------------------ compute warps ------------------------------
+    const int cw = warp - 2;          // 0..NCW-1
+    const int quarter = warp & 3;     // TMEM lane quarter = keys quarter*32 .. +31 of a tile
+    const int half = cw >> 2;         // this warp's WROWS of the quarter's 32 keys
+    const int t = threadIdx.x - 64;   // 0..32*NCW-1
+    const bool own = lane / WROWS == half;
+    constexpr int DV = Gm::DV;
+    // (p, p) pairs of the warp's rows: [WROWS][G]
+    unsigned long long *pw = reinterpret_cast<unsigned long long *>(smem + Gm::OFF_P) + cw * WROWS * G;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    // this lane's byte offset inside a row of a V tile (128-byte swizzle undone per row)
+    const int vchunk = D == 128 ? lane >> 1 : lane >> 2;
+    const int vkb = vchunk >> 3, vci = vchunk & 7;
+    const int vsub = D == 128 ? (lane & 1) * 8 : (lane & 3) * 4;
+    int it = 0, sc = 0;
+    bool ok = true;
+    // q of unit uu into operand buffer qb: rows 0..G-1, one 16-byte chunk per thread
+    auto write_q = [&](int uu, int qb) {
+      uint8_t *qo = smem + Gm::OFF_Q + qb * Gm::QOP;
+      for (int c = t; c < G * D / 8; c += 32 * NCW) {
+        const int g = c / (D / 8), ch = c % (D / 8), kb = ch >> 3, ci = ch & 7;
+        *reinterpret_cast<uint4 *>(qo + kb * Gm::QBLK + g * 128 + ((ci ^ (g & 7)) << 4)) =
+            *reinterpret_cast<const uint4 *>(p.q + ((size_t)uu * G + g) * D + ch * 8);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar + B_QFULL + 8 * qb);
+    };
+    if (nu > 0) write_q(unit_at(0), 0);
+    if (nu > 1) write_q(unit_at(1), 1);
+    for (int k = 0; k < nu; ++k) {
+      const int u = unit_at(k);
+      const Seg sg = seg_geo(p, u, b, s0, s1, T, Q, R, t == 0);
+      // the next unit's q goes where the previous unit's was, once the MMAs of the
+      // previous unit have completed (it may have had no tiles here, so its S^T reads
+      // prove nothing)
+      if (k > 0 && k + 1 < nu) {
+        ok = __all_sync(0xffffffffu, ok && ab.wait(bar + B_QEMPTY + 8 * ((k - 1) & 1), ((k - 1) >> 1) & 1));
+        if (ok) write_q(unit_at(k + 1), (k + 1) & 1);
+      }
+      // running max (the same on every lane: it covers the quarter's 32 keys), and per
+      // lane the normaliser of its own key rows and o over its head-dim slice
+      float m_run[G], l_run[G];
+      unsigned long long o2[G][DV / 2];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const uint4 w = got ? *reinterpret_cast<const uint4 *>(qsm + (g * D + sl * 8) * 2)
-                            : make_uint4(0, 0, 0, 0);
-        qr[g][0] = pk(bf_lo(w.x) * p.c, bf_hi(w.x) * p.c);
-        qr[g][1] = pk(bf_lo(w.y) * p.c, bf_hi(w.y) * p.c);
-        qr[g][2] = pk(bf_lo(w.z) * p.c, bf_hi(w.z) * p.c);
-        qr[g][3] = pk(bf_lo(w.w) * p.c, bf_hi(w.w) * p.c);
+        m_run[g] = -INFINITY;
+        l_run[g] = 0.f;
+#pragma unroll
+        for (int d = 0; d < DV / 2; ++d) o2[g][d] = 0ull;
       }
-      __syncwarp();
-      if (got && lane == 0) mbar_arrive(bar + 80 + 8 * qb);
-    }
-    float m_run[G], l_run[G];
-    unsigned long long o2[G][DV / 2];
+      const int nrows = sg.r1 - sg.r0;
+      const int ntiles = (nrows + ROWS - 1) / ROWS;
+      const int arow_local = sg.arow - sg.r0;
+      for (int i = 0; i < ntiles; ++i, ++sc) {
+        // ---------------- logits of this lane's key, from TMEM ----------------
+        float lg[G];
+        {
+          const int sbf = sc & 1;
+          const bool got = __all_sync(0xffffffffu, ok && ab.wait(bar + B_SFULL + 8 * sbf, (sc >> 1) & 1));
+          ok = got;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      m_run[g] = -INFINITY;
-      l_run[g] = 0.f;
+          for (int g = 0; g < G; ++g) lg[g] = -INFINITY;
+          if (got) {
+            tc_fence_after();
+            float s8[8];
+            tmem_ld8(tmem + lane_base + (uint32_t)(sbf * QN), s8);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + B_SEMPTY + 8 * sbf);
+            if (i * ROWS + quarter * 32 + lane < nrows)
 #pragma unroll
-      for (int d = 0; d < DV / 2; ++d) o2[g][d] = 0ull;
-    }
-    const int nrows = sg.r1 - sg.r0;
-    const int ntiles = (nrows + ROWS - 1) / ROWS;
-    const int arow_local = sg.arow - sg.r0;
-    for (int i = 0; i < ntiles; ++i, it += 2) {
-      const int arr = arow_local - i * ROWS;
-      const bool patched = sg.arow >= 0 && arr >= 0 && arr < ROWS;  // same for the CTA
-      const int wrows = min(WROWS, nrows - i * ROWS - cw * WROWS);   // this warp's rows (<= 0: none)
-      // ---------------- K half: logits of the warp's rows ----------------
-      float lg[NPASS];
-      {
-        const int st = it % NST;
-        const bool got = __all_sync(0xffffffffu, ok && ab.wait(bar + 8 * st, (it / NST) & 1));
-        ok = got;
-        uint8_t *tile = smem + Gm::OFF_RING + st * Gm::TB;
-        if (patched) {  // every compute thread reaches this barrier
-          if (got) patch_row<D>(tile, p.k_new + (size_t)u * D, arr, t);
-          named_bar(1, 128);
+              for (int g = 0; g < G; ++g) lg[g] = s8[g] * p.c;
+          }
         }
+        // ------- online softmax: one warp max per head, no per-tile sums -------
+        bool grew = false;
+        float f[G];
 #pragma unroll
-        for (int pass = 0; pass < NPASS; ++pass) lg[pass] = -INFINITY;
-        if (got) {
+        for (int g = 0; g < G; ++g) {
+          float mx;
+          asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx) : "f"(lg[g]));
+          const float mnew = fmaxf(m_run[g], mx);
+          grew |= mnew > m_run[g];
+          f[g] = mnew > m_run[g] ? (m_run[g] == -INFINITY ? 0.f : ex2(m_run[g] - mnew)) : 1.f;
+          const float e = mnew == -INFINITY ? 0.f : ex2(lg[g] - mnew);  // ex2(-inf) = 0
+          if (own) pw[(lane % WROWS) * G + g] = pk(e, e);
+          l_run[g] = l_run[g] * f[g] + (own ? e : 0.f);
+          m_run[g] = mnew;
+        }
+        if (grew) {  // warp-uniform: the maxima are the same on every lane
 #pragma unroll
-          for (int pass = 0; pass < NPASS; ++pass) {
-            const int r = cw * WROWS + pass * RPW + rg;  // row of the tile
-            // chunk sl: k-block sl / 8, slot sl % 8 (the 8 lanes of a phase hit 8 slots)
-            const uint4 w = *reinterpret_cast<const uint4 *>(
-                tile + (sl >> 3) * Gm::KBLK + r * 128 + (((sl & 7) ^ (r & 7)) << 4));
-            const unsigned long long k01 = bf2(w.x), k23 = bf2(w.y), k45 = bf2(w.z),
-                                     k67 = bf2(w.w);
-            float v[G];
+          for (int g = 0; g < G; ++g) {
+            const unsigned long long ff = pk(f[g], f[g]);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-              unsigned long long acc = 0ull;
-              ffma2(acc, qr[g][0], k01);
-              ffma2(acc, qr[g][1], k23);
-              ffma2(acc, qr[g][2], k45);
-              ffma2(acc, qr[g][3], k67);
-              const float2 a = upk(acc);
-              v[g] = a.x + a.y;
+            for (int d = 0; d < DV / 2; ++d) {
+              unsigned long long z = 0ull;
+              ffma2(z, o2[g][d], ff);
+              o2[g][d] = z;
             }
-            // transpose-reduce over the row's TPR lanes: each split level halves the heads a
-            // lane keeps (the lane's bits at those levels name the head it keeps, myhead)
-#pragma unroll
-            for (int lvl = TPR / 2, nv = G; lvl >= 1; lvl >>= 1) {
-              if (nv >= 2) {
-                const bool upper = (lane & lvl) != 0;
-#pragma unroll
-                for (int x = 0; x < G / 2; ++x) {
-                  if (x < nv / 2) {
-                    const float send = upper ? v[x] : v[x + nv / 2];
-                    const float keep = upper ? v[x + nv / 2] : v[x];
-                    v[x] = keep + __shfl_xor_sync(0xffffffffu, send, lvl);
-                  }
-                }
-                nv /= 2;
+          }
+        }
+        __syncwarp();  // probabilities visible to the whole warp
+        // ---------------- V half: o[g] += p[row][g] * v[row] ----------------
+        {
+          const int j = it + 2 * i + 1, st = j % NST;
+          bool got = __all_sync(0xffffffffu, ok && ab.wait(bar + B_FULL + 8 * st, (j / NST) & 1));
+          // self-check of the ring protocol: the stage must hold this tile
+          if (got && !__all_sync(0xffffffffu, tag[st] == j)) {
+            if (lane == 0) {
+              set_status(p.status, KVC_DEV_BAD_STATE);
+              *abort_flag = 1;
+            }
+            got = false;
+          }
+          ok = got;
+          uint8_t *tile = smem + Gm::OFF_RING + st * Gm::TB;
+          const int arr = arow_local - i * ROWS;
+          const bool patched = sg.arow >= 0 && arr >= 0 && arr < ROWS;  // same for the CTA
+          if (patched) {  // every compute thread reaches this barrier
+            if (got) patch_row<D>(tile, p.v_new + (size_t)u * D, arr, t);
+            named_bar(1, 32 * NCW);
+          }
+          const int r0 = quarter * 32 + half * WROWS;              // first own row of the tile
+          const int wrows = min(WROWS, nrows - i * ROWS - r0);      // own rows (<= 0: none)
+          if (got) {
+            const uint8_t *vrow = tile + vkb * Gm::KBLK + r0 * 128 + vsub;
+            auto row = [&](int i2) {
+              // r0 is a multiple of 8, so the row's swizzle phase is i2 & 7
+              const uint8_t *src = vrow + i2 * 128 + ((vci ^ (i2 & 7)) << 4);
+              unsigned long long v01, v23 = 0ull;
+              if (D == 128) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(src);
+                v01 = bf2(w.x);
+                v23 = bf2(w.y);
               } else {
-                v[0] += __shfl_xor_sync(0xffffffffu, v[0], lvl);
+                v01 = bf2(*reinterpret_cast<const uint32_t *>(src));
+              }
+              const unsigned long long *pr = pw + i2 * G;
+#pragma unroll
+              for (int g = 0; g < G; g += 2) {
+                unsigned long long pp0, pp1 = 0ull;
+                if (G >= 2) {
+                  const ulonglong2 q2 = *reinterpret_cast<const ulonglong2 *>(pr + g);
+                  pp0 = q2.x;
+                  pp1 = q2.y;
+                } else {
+                  pp0 = pr[g];
+                }
+                ffma2(o2[g][0], pp0, v01);
+                if (DV == 4) ffma2(o2[g][DV / 2 - 1], pp0, v23);
+                if (G >= 2) {
+                  ffma2(o2[g + 1 < G ? g + 1 : g][0], pp1, v01);
+                  if (DV == 4) ffma2(o2[g + 1 < G ? g + 1 : g][DV / 2 - 1], pp1, v23);
+                }
+              }
+            };
+            if (wrows == WROWS) {
+#pragma unroll
+              for (int i2 = 0; i2 < WROWS; ++i2) row(i2);
+            } else {
+#pragma unroll 4
+              for (int i2 = 0; i2 < WROWS; ++i2) {
+                if (i2 >= wrows) break;
+                row(i2);
               }
             }
-            if (pass * RPW + rg < wrows) lg[pass] = v[0];
+            if (patched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + B_EMPTY + 8 * st);
           }
-          if (patched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar + 32 + 8 * st);  // the K stage may be refilled
+          __syncwarp();  // pw is rewritten by the next tile
         }
       }
-      // ------- online softmax of the warp's rows (no other warp is involved) -------
-      float mnew[G], f[G];
-      {
-        float tmax = lg[0];
+      it += 2 * ntiles;
+      // ---- hand the warp's (max, normaliser, o) of this segment to the epilogue ----
+      float lw[G];
 #pragma unroll
-        for (int pass = 1; pass < NPASS; ++pass) tmax = fmaxf(tmax, lg[pass]);
-        // lanes holding the same head differ in the row bits (lane / TPR)
+      for (int g = 0; g < G; ++g) {
+        float sum = l_run[g];
 #pragma unroll
-        for (int o = TPR; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-        if (head_writer) wxw[myhead] = tmax;
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        lw[g] = sum;
+      }
+      const int rb = k & 1;
+      if (k >= 2)  // the epilogue has finished with segment k - 2's buffer
+        ok = __all_sync(0xffffffffu, ok && ab.wait(bar + B_REMPTY + 8 * rb, ((k - 2) >> 1) & 1));
+      if (ok) {
+        float *stg = reinterpret_cast<float *>(smem + Gm::OFF_STAGE) + ((size_t)rb * NCW + cw) * G * D;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          if (DV == 4) {
+            const float2 a = upk(o2[g][0]), c2 = upk(o2[g][DV / 2 - 1]);
+            *reinterpret_cast<float4 *>(stg + g * D + lane * 4) = make_float4(a.x, a.y, c2.x, c2.y);
+          } else {
+            *reinterpret_cast<float2 *>(stg + g * D + lane * 2) = upk(o2[g][0]);
+          }
+        }
+        if (lane == 0) {
+          float2 *sst = reinterpret_cast<float2 *>(smem + Gm::OFF_SST) + ((size_t)rb * NCW + cw) * G;
+#pragma unroll
+          for (int g = 0; g < G; ++g) sst[g] = make_float2(m_run[g], lw[g]);
+        }
         __syncwarp();
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          mnew[g] = fmaxf(m_run[g], wxw[g]);
-          f[g] = m_run[g] == -INFINITY ? 0.f : ex2(m_run[g] - mnew[g]);  // rescale of the past
-        }
-        __syncwarp();  // wxw is reused for the sums
-        float mh = mnew[0];
-#pragma unroll
-        for (int g = 1; g < G; ++g)
-          if (myhead == g) mh = mnew[g];
-        float ps = 0.f;
-#pragma unroll
-        for (int pass = 0; pass < NPASS; ++pass) {
-          const float e = lg[pass] == -INFINITY ? 0.f : ex2(lg[pass] - mh);
-          ps += e;
-          if (row_writer) pw[(pass * RPW + rg) * G + myhead] = e;
-        }
-#pragma unroll
-        for (int o = TPR; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-        if (head_writer) wxw[myhead] = ps;
-        __syncwarp();  // sums and probabilities visible to the whole warp
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          l_run[g] = l_run[g] * f[g] + wxw[g];
-          m_run[g] = mnew[g];
-          const unsigned long long ff = pk(f[g], f[g]);
-#pragma unroll
-          for (int d = 0; d < DV / 2; ++d) {
-            unsigned long long z = 0ull;
-            ffma2(z, o2[g][d], ff);
-            o2[g][d] = z;
-          }
-        }
-      }
-      // ---------------- V half: o[g] += p[row][g] * v[row] ----------------
-      {
-        const int st = (it + 1) % NST;
-        const bool got = __all_sync(0xffffffffu, ok && ab.wait(bar + 8 * st, ((it + 1) / NST) & 1));
-        ok = got;
-        uint8_t *tile = smem + Gm::OFF_RING + st * Gm::TB;
-        if (patched) {
-          if (got) patch_row<D>(tile, p.v_new + (size_t)u * D, arr, t);
-          named_bar(1, 128);
-        }
-        if (got) {
-#pragma unroll 4
-          for (int i2 = 0; i2 < WROWS; ++i2) {
-            if (i2 >= wrows) break;
-            const int rr = cw * WROWS + i2;
-            unsigned long long v01, v23 = 0ull;
-            if (D == 128) {
-              const int chunk = lane >> 1, kb = chunk >> 3, ci = chunk & 7;
-              const uint2 w = *reinterpret_cast<const uint2 *>(
-                  tile + kb * Gm::KBLK + rr * 128 + ((ci ^ (rr & 7)) << 4) + (lane & 1) * 8);
-              v01 = bf2(w.x);
-              v23 = bf2(w.y);
-            } else {
-              const int ci = lane >> 2;
-              const uint32_t w = *reinterpret_cast<const uint32_t *>(
-                  tile + rr * 128 + ((ci ^ (rr & 7)) << 4) + (lane & 3) * 4);
-              v01 = bf2(w);
-            }
-            const float *pr = pw + i2 * G;
-            float pv[G];
-            if (G >= 4) {
-#pragma unroll
-              for (int g = 0; g < G; g += 4) {
-                const float4 q4 = *reinterpret_cast<const float4 *>(pr + g);
-                pv[g] = q4.x;
-                pv[(g + 1) % G] = q4.y;
-                pv[(g + 2) % G] = q4.z;
-                pv[(g + 3) % G] = q4.w;
-              }
-            } else {
-#pragma unroll
-              for (int g = 0; g < G; ++g) pv[g] = pr[g];
-            }
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const unsigned long long pp = pk(pv[g], pv[g]);
-              ffma2(o2[g][0], pp, v01);
-              if (DV == 4) ffma2(o2[g][DV / 2 - 1], pp, v23);
-            }
-          }
-          if (patched) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar + 32 + 8 * st);
-        }
-        __syncwarp();  // pw and wxw are rewritten by the next tile
+        if (lane == 0) mbar_arrive(bar + B_RFULL + 8 * rb);
       }
     }
-    // ---- merge the four warps' (max, normaliser, o) of this segment ----
-    if (lane == 0)
+  } else {
+    // --------------- epilogue warps: merge each segment's staged warp states ---------------
+    constexpr int NE = 32 * NEW;
+    const int te = threadIdx.x - EPI0;  // 0..NE-1
+    volatile int *eok_flag = reinterpret_cast<volatile int *>(smem + Gm::OFF_BAR + B_EOK);
+    float *scl = reinterpret_cast<float *>(smem + Gm::OFF_SCL);     // [NCW][G]
+    float2 *mlv = reinterpret_cast<float2 *>(smem + Gm::OFF_ML);    // [G] (M, L)
+    for (int k = 0; k < nu; ++k) {
+      const int u = unit_at(k), rb = k & 1;
+      const Seg sg = seg_geo(p, u, b, s0, s1, T, Q, R, false);
+      if (te == 0) *eok_flag = ab.wait(bar + B_RFULL + 8 * rb, (k >> 1) & 1) ? 1 : 0;
+      named_bar(2, NE);
+      const bool eok = *eok_flag != 0;  // the same for the whole group
+      const float2 *sst = reinterpret_cast<const float2 *>(smem + Gm::OFF_SST) + (size_t)rb * NCW * G;
+      const float *stg = reinterpret_cast<const float *>(smem + Gm::OFF_STAGE) + (size_t)rb * NCW * G * D;
+      if (eok && te < G) {  // the segment's max and normaliser per head, and warp weights
+        const int g = te;
+        float M = -INFINITY;
 #pragma unroll
-      for (int g = 0; g < G; ++g) wst[cw * G + g] = make_float2(m_run[g], l_run[g]);
-    named_bar(1, 128);
-    float Mg[G], Lg[G];
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, sst[w * G + g].x);
+        float L = 0.f;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float M = -INFINITY;
-#pragma unroll
-      for (int w2 = 0; w2 < NCW; ++w2) M = fmaxf(M, wst[w2 * G + g].x);
-      float L = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w2 = 0; w2 < NCW; ++w2) {
-          const float2 ml = wst[w2 * G + g];
-          if (ml.x != -INFINITY) L += ml.y * ex2(ml.x - M);
+        for (int w = 0; w < NCW; ++w) {
+          const float2 ml = sst[w * G + g];
+          const float s = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+          scl[w * G + g] = s;
+          L += ml.y * s;
         }
+        mlv[g] = make_float2(M, L);
       }
-      Mg[g] = M;
-      Lg[g] = L;
-      const float fw = m_run[g] == -INFINITY ? 0.f : ex2(m_run[g] - M);
-#pragma unroll
-      for (int d = 0; d < DV / 2; ++d) {
-        const float2 v = upk(o2[g][d]);
-        atomicAdd(&red[g * D + lane * DV + 2 * d], v.x * fw);
-        atomicAdd(&red[g * D + lane * DV + 2 * d + 1], v.y * fw);
-      }
-    }
-    named_bar(1, 128);
-    const bool direct = sg.nseg == 1;
-    for (int e = t; e < G * D; e += 128) {
-      const int g = e / D, d = e - g * D;
-      float M = Mg[0], L = Lg[0];
-#pragma unroll
-      for (int h = 1; h < G; ++h)
-        if (g == h) {
-          M = Mg[h];
-          L = Lg[h];
-        }
-      const float O = red[e];
-      red[e] = 0.f;  // ready for the next segment (only this thread touches element e here)
-      if (direct) {
-        p.out[(size_t)u * G * D + e] = __float2bfloat16(L > 0.f ? O / L : 0.f);
-        if (e < D / 8 && sg.arow >= 0) append_row<D>(p, u, sg.arow, sg.n_old, e);
-      } else {
-        p.part_o[(((size_t)u * T + sg.iseg) * G + g) * D + d] = O;
-        if (d == 0) p.part_ml[((size_t)u * T + sg.iseg) * G + g] = make_float2(M, L);
-      }
-    }
-    if (!direct) {
-      __threadfence();
-      named_bar(1, 128);
-      if (t == 0) *last_flag = (atomicAdd(&p.cnt[u], 1) == sg.nseg - 1);
-      named_bar(1, 128);
-      if (*last_flag) {
-        __threadfence();
-        for (int e = t; e < G * D; e += 128) {
+      named_bar(2, NE);
+      const bool direct = sg.nseg == 1;
+      if (eok) {
+        for (int e = te; e < G * D; e += NE) {
           const int g = e / D, d = e - g * D;
-          // independent loads (batched by unrolling), then the merge
-          float M = -INFINITY;
-#pragma unroll 4
-          for (int s2 = 0; s2 < sg.nseg; ++s2)
-            M = fmaxf(M, __ldcg(p.part_ml + ((size_t)u * T + s2) * G + g).x);
-          float L = 0.f, O = 0.f;
-          if (M != -INFINITY) {
-#pragma unroll 4
-            for (int s2 = 0; s2 < sg.nseg; ++s2) {
-              const float2 ml = __ldcg(p.part_ml + ((size_t)u * T + s2) * G + g);
-              const float o = __ldcg(p.part_o + (((size_t)u * T + s2) * G + g) * D + d);
-              const float fs = ml.y > 0.f ? ex2(ml.x - M) : 0.f;  // empty segments add 0
-              L += ml.y * fs;
-              O += o * fs;
-            }
+          float O = 0.f;
+#pragma unroll
+          for (int w = 0; w < NCW; ++w) O += stg[(size_t)w * G * D + e] * scl[w * G + g];
+          const float2 ml = mlv[g];
+          if (direct) {
+            p.out[(size_t)u * G * D + e] = __float2bfloat16(ml.y > 0.f ? O / ml.y : 0.f);
+            if (e < D / 8 && sg.arow >= 0) append_row<D>(p, u, sg.arow, sg.n_old, e);
+          } else {
+            p.part_o[(((size_t)u * T + sg.iseg) * G + g) * D + d] = O;
+            if (d == 0) p.part_ml[((size_t)u * T + sg.iseg) * G + g] = ml;
           }
-          p.out[(size_t)u * G * D + e] = __float2bfloat16(L > 0.f ? O / L : 0.f);
         }
-        if (sg.arow >= 0)
-          for (int e = t; e < D / 8; e += 128) append_row<D>(p, u, sg.arow, sg.n_old, e);
-        if (t == 0) p.cnt[u] = 0;
+      }
+      named_bar(2, NE);  // the staged states, weights and (M, L) have been read
+      if (te == 0) mbar_arrive(bar + B_REMPTY + 8 * rb);
+      if (eok && !direct) {
+        __threadfence();
+        named_bar(2, NE);
+        if (te == 0) *last_flag = (atomicAdd(&p.cnt[u], 1) == sg.nseg - 1);
+        named_bar(2, NE);
+        if (*last_flag) {
+          __threadfence();
+          for (int e = te; e < G * D; e += NE) {
+            const int g = e / D, d = e - g * D;
+            // independent loads (batched by unrolling), then the merge
+            float M = -INFINITY;
+#pragma unroll 4
+            for (int s2 = 0; s2 < sg.nseg; ++s2)
+              M = fmaxf(M, __ldcg(p.part_ml + ((size_t)u * T + s2) * G + g).x);
+            float L = 0.f, O = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll 4
+              for (int s2 = 0; s2 < sg.nseg; ++s2) {
+                const float2 ml = __ldcg(p.part_ml + ((size_t)u * T + s2) * G + g);
+                const float o = __ldcg(p.part_o + (((size_t)u * T + s2) * G + g) * D + d);
+                const float fs = ml.y > 0.f ? ex2(ml.x - M) : 0.f;  // empty segments add 0
+                L += ml.y * fs;
+                O += o * fs;
+              }
+            }
+            p.out[(size_t)u * G * D + e] = __float2bfloat16(L > 0.f ? O / L : 0.f);
+          }
+          if (sg.arow >= 0)
+            for (int e = te; e < D / 8; e += NE) append_row<D>(p, u, sg.arow, sg.n_old, e);
+          if (te == 0) p.cnt[u] = 0;
+        }
+        named_bar(2, NE);  // last_flag is reused by the next segment
       }
     }
-    named_bar(1, 128);  // qs, red and last_flag are reused by the next segment
   }
+
+  // ---------------------------------- teardown ----------------------------------
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 template <int D, int G>
