@@ -45,6 +45,8 @@ constexpr int NTHREADS = 32 * NWARPS;
 constexpr int TMEM_COLS = 512;  // 4 accumulators of 128 fp32 columns
 constexpr int LEAD = 2;         // pass-1 tiles of a round issued before its first pass-2 tile
 constexpr int XB = 20;          // partial statistics loaded per batch (group sizes up to 20: one)
+constexpr int TR_ROWS = 32;     // row tiles up to this size run pass 1 transposed (keys on lanes)
+constexpr float TR_SLACK = 8.f; // transposed pass 1 moves a row's reference only past this (log2)
 
 template <int D>
 struct Geo {
@@ -277,6 +279,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
       int kit = 0, qcnt[NQ] = {};
+      const uint64_t pol_keep = l2_policy_evict_last(), pol_drop = l2_policy_evict_first();
       bool ok = true;
       for (int k = 0; k < njobs + LAG && ok; ++k) {
         Job Ja{}, Jb{};
@@ -300,7 +303,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int ia = 0, ib = 0; ia < na || ib < nb;) {
           int row;
-          if (next_is_a(ia, ib, na, nb)) {
+          const bool is_a = next_is_a(ia, ib, na, nb);
+          if (is_a) {
             row = Ja.u * p.L + (Ja.t0 + ia) * TILE;
             ++ia;
           } else {
@@ -311,9 +315,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (!ab.wait(ctl + C_KEMPTY + 8 * s, (use & 1) ^ 1)) { ok = false; break; }
           tag[s] = kit;  // this stage's phase now belongs to tile kit
           mbar_arrive_expect_tx(ctl + C_KFULL + 8 * s, G::TILE_BYTES);
+          // a pass-1 load is read again by pass 2 (keep it in L2); a pass-2 load is the
+          // tile's last use (let it go first)
           for (int kb = 0; kb < G::KB; ++kb)
-            tma_load_2d(sK + s * G::TILE_BYTES + kb * G::KBLK, &tk, kb * 64, row,
-                        ctl + C_KFULL + 8 * s);
+            tma_load_2d_hint(sK + s * G::TILE_BYTES + kb * G::KBLK, &tk, kb * 64, row,
+                             ctl + C_KFULL + 8 * s, is_a ? pol_keep : pol_drop);
           ++kit;
         }
       }
@@ -353,7 +359,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           ++qcnt[qb];
           tc_fence_after();
         }
-        const uint32_t idesc = idesc_bf16(128, mine_a ? TILE : (Jb.rpad > 0 ? Jb.rpad : 16));
+        // pass 1 of a job with at most TR_ROWS query rows also uses the transposed product
+        // S^T = K . Q^T (keys on TMEM lanes), like pass 2
+        const bool tra = mine_a && Ja.rpad <= TR_ROWS;
+        const uint32_t idesc = idesc_bf16(128, mine_a ? (tra ? Ja.rpad : TILE) : (Jb.rpad > 0 ? Jb.rpad : 16));
         const uint64_t qd = sdesc_k128(sQ + qb * G::TILE_BYTES);
         for (int ia = 0, ib = 0; ia < na || ib < nb;) {
           const bool isa = next_is_a(ia, ib, na, nb);
@@ -373,7 +382,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // descriptors of the tile's first 16-wide k-step; later k-steps advance the
           // start address field (bytes / 16) by a constant
           const uint64_t kd = sdesc_k128(sK + s * G::TILE_BYTES);
-          const uint64_t ad = mine_a ? qd : kd, bd = mine_a ? kd : qd;
+          const uint64_t ad = (mine_a && !tra) ? qd : kd, bd = (mine_a && !tra) ? kd : qd;
 #pragma unroll
           for (int kb = 0; kb < G::KB; ++kb) {
 #pragma unroll
@@ -410,54 +419,128 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int n = J.t1 - J.t0;
       const bool rvalid = lrow < J.nrows;
       const int prow = rvalid ? p.L - p.Wq + (J.rho0 + lrow) % p.Wq : -1;
-      const bool warp_active = quarter * 32 < J.nrows;
       float m = -INFINITY, z = 0.f;
-      for (int i = 0; i < n; ++i, ++it1) {
-        const int b = it1 & 1;
-        const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_SFULL + 8 * b, (it1 >> 1) & 1));
-        ok = got;
-        if (!got) continue;
-        tc_fence_after();
-        if (warp_active) {
-          const int kbase = (J.t0 + i) * TILE + ch * 64;
-          float s[64];
-          tmem_ld32(tmem + lane_base + (uint32_t)(b * 128 + ch * 64), s);
-          tmem_ld32(tmem + lane_base + (uint32_t)(b * 128 + ch * 64 + 32), s + 32);
-          tmem_wait_ld();
-          if (kbase + 63 > prow) {
+      if (J.rpad <= TR_ROWS) {
+        // ---- transposed: keys on TMEM lanes, this warp's 16 rows in registers ----
+        // Per row a warp-wide max (redux) moves the row's reference only when the max
+        // passes it by TR_SLACK, and each lane keeps its own partial normaliser; the
+        // lanes and the four key quarters are summed once per job.
+        const bool wact = ch * 16 < J.rpad;  // warp-uniform
+        const bool padrows = J.nrows < J.rpad;
+        float tm[16], tl[16];
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (kbase + c > prow) s[c] = -INFINITY;
-          }
-          const float mnew = fmaxf(m, max64(s) * p.c);
-          if (mnew != -INFINITY) {
-            // exp2(s * c - m) summed in packed fp32x2 pairs, four independent chains
-            const unsigned long long cc = pk(p.c, p.c), nm = pk(-mnew, -mnew);
-            unsigned long long a[4] = {0ull, 0ull, 0ull, 0ull};
+        for (int r = 0; r < 16; ++r) {
+          tm[r] = -INFINITY;
+          tl[r] = 0.f;
+        }
+        for (int i = 0; i < n; ++i, ++it1) {
+          const int b = it1 & 1;
+          const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_SFULL + 8 * b, (it1 >> 1) & 1));
+          ok = got;
+          if (!got) continue;
+          tc_fence_after();
+          if (wact) {
+            float s[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)(b * 128 + ch * 16), s);
+            tmem_wait_ld();
+            const int key = (J.t0 + i) * TILE + quarter * 32 + lane;
+            if (padrows || key > J.pmin) {  // causal mask inside the window, padding rows
 #pragma unroll
-            for (int c = 0; c < 64; c += 8) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float2 x = upk(fma2(pk(s[c + 2 * q], s[c + 2 * q + 1]), cc, nm));
-                a[q] = add2(a[q], pk(ex2(x.x), ex2(x.y)));
+              for (int r = 0; r < 16; ++r) {
+                const int row = ch * 16 + r;
+                const int pr = row < J.nrows ? p.L - p.Wq + (J.rho0 + row) % p.Wq : -1;
+                if (key > pr) s[r] = -INFINITY;
               }
             }
-            z = z * ex2(m - mnew) + sum4(a);
-            m = mnew;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+              float mx;
+              asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx) : "f"(s[r]));
+              mx *= p.c;                    // c > 0: the max of the scaled logits
+              if (mx > tm[r] + TR_SLACK) {  // warp-uniform
+                tl[r] *= ex2(tm[r] - mx);   // ex2(-inf) = 0 for a first reference
+                tm[r] = mx;
+              }
+            }
+            const unsigned long long cc = pk(p.c, p.c);
+#pragma unroll
+            for (int r = 0; r < 16; r += 2) {
+              const float o0 = tm[r] == -INFINITY ? -INFINITY : -tm[r];
+              const float o1 = tm[r + 1] == -INFINITY ? -INFINITY : -tm[r + 1];
+              const float2 x = upk(fma2(pk(s[r], s[r + 1]), cc, pk(o0, o1)));
+              const float2 t = upk(add2(pk(tl[r], tl[r + 1]), pk(ex2(x.x), ex2(x.y))));
+              tl[r] = t.x;
+              tl[r + 1] = t.y;
+            }
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ctl + C_SEMPTY + 8 * b);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(ctl + C_SEMPTY + 8 * b);
+        float2 *ts = hstat + (k & 1) * TILE;  // [key quarter][32 rows]
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          float v = tl[r];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (wact && lane == r) ts[quarter * 32 + ch * 16 + r] = make_float2(tm[r], v);
+        }
+        named_bar(2, 256);
+        if (ch == 0 && lrow < J.rpad)  // quarter 0's lanes: one row each
+#pragma unroll
+          for (int q = 0; q < 4; ++q) merge_stat(m, z, ts[q * 32 + lrow]);
+      } else {
+        const bool warp_active = quarter * 32 < J.nrows;
+        for (int i = 0; i < n; ++i, ++it1) {
+          const int b = it1 & 1;
+          const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_SFULL + 8 * b, (it1 >> 1) & 1));
+          ok = got;
+          if (!got) continue;
+          tc_fence_after();
+          if (warp_active) {
+            const int kbase = (J.t0 + i) * TILE + ch * 64;
+            float s[64];
+            tmem_ld32(tmem + lane_base + (uint32_t)(b * 128 + ch * 64), s);
+            tmem_ld32(tmem + lane_base + (uint32_t)(b * 128 + ch * 64 + 32), s + 32);
+            tmem_wait_ld();
+            if (kbase + 63 > prow) {
+#pragma unroll
+              for (int c = 0; c < 64; ++c)
+                if (kbase + c > prow) s[c] = -INFINITY;
+            }
+            const float mnew = fmaxf(m, max64(s) * p.c);
+            if (mnew != -INFINITY) {
+              // exp2(s * c - m) summed in packed fp32x2 pairs, four independent chains
+              const unsigned long long cc = pk(p.c, p.c), nm = pk(-mnew, -mnew);
+              unsigned long long a[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+              for (int c = 0; c < 64; c += 8) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const float2 x = upk(fma2(pk(s[c + 2 * q], s[c + 2 * q + 1]), cc, nm));
+                  a[q] = add2(a[q], pk(ex2(x.x), ex2(x.y)));
+                }
+              }
+              z = z * ex2(m - mnew) + sum4(a);
+              m = mnew;
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ctl + C_SEMPTY + 8 * b);
+        }
+        // ---- merge the two column halves ----
+        if (ch == 1) hstat[(k & 1) * TILE + lrow] = make_float2(m, z);
+        named_bar(2, 256);
+        if (ch == 0) {
+          const float2 o = hstat[(k & 1) * TILE + lrow];
+          const float mn = fmaxf(m, o.x);
+          if (mn != -INFINITY) z = z * ex2(m - mn) + o.y * ex2(o.x - mn);
+          m = mn;
+        }
       }
-      // ---- merge the two column halves, then publish this job's row statistics ----
-      if (ch == 1) hstat[(k & 1) * TILE + lrow] = make_float2(m, z);
-      named_bar(2, 256);
+      // ---- publish this job's row statistics ----
       if (ch == 0) {
-        const float2 o = hstat[(k & 1) * TILE + lrow];
-        const float mn = fmaxf(m, o.x);
-        if (mn != -INFINITY) z = z * ex2(m - mn) + o.y * ex2(o.x - mn);
-        m = mn;
         if (p.g == 1) {
           const int xb = k & 1;
           const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_XEMPTY + 8 * xb, ((k >> 1) & 1) ^ 1));
@@ -491,7 +574,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int j = gamma + k * p.ngroups;
       const Job J = job_geo(p, j, xg);
       const int n = J.t1 - J.t0;
-      // statistics of this job -> per-row offsets (threads 0..127, i.e. the rh == 0 warps)
+      // statistics of this job -> per-row offsets in shared memory
       float M = 0.f, Z = 0.f;
       if (p.g == 1) {
         if (rh == 0) {
@@ -517,21 +600,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         named_bar(3, 256);
         ok = ok && (*go != 0);
-        if (t2 < TILE && ok) {
-          // combine the g partials of this row (in CTA order), up to XB loads in flight
-          const float2 *src = p.part + (size_t)j * p.g * TILE + t2;
-          M = -INFINITY;
-          for (int r = 0; r < p.g; r += XB) {
+        // combine the g partials of each live row: tpr consecutive threads per row, each
+        // over a strided share of the CTAs with up to XB loads in flight, then merged by
+        // shuffles (a fixed order, so the result is the same on every call)
+        const int tpr = J.nrows <= 32 ? 8 : (J.nrows <= 64 ? 4 : 2);  // tpr * rows <= 256
+        const int row = t2 / tpr, sub = t2 - row * tpr;
+        M = -INFINITY;
+        if (row < J.nrows && ok) {
+          const float2 *src = p.part + (size_t)j * p.g * TILE + row;
+          for (int r = sub; r < p.g; r += XB * tpr) {
             float2 v[XB];
 #pragma unroll
             for (int i = 0; i < XB; ++i)
-              v[i] = r + i < p.g ? __ldcg(src + (size_t)(r + i) * TILE) : make_float2(-INFINITY, 0.f);
+              v[i] = r + i * tpr < p.g ? __ldcg(src + (size_t)(r + i * tpr) * TILE)
+                                       : make_float2(-INFINITY, 0.f);
 #pragma unroll
             for (int i = 0; i < XB; ++i) merge_stat(M, Z, v[i]);
           }
         }
+        for (int o = 1; o < tpr; o <<= 1) {
+          const float Mo = __shfl_xor_sync(0xffffffffu, M, o), Zo = __shfl_xor_sync(0xffffffffu, Z, o);
+          merge_stat(M, Z, make_float2(Mo, Zo));
+        }
+        if (sub == 0 && row < J.nrows) {
+          noff[row] = Z > 0.f ? -(M + lg2(Z)) : -INFINITY;
+          rowpos[row] = p.L - p.Wq + (J.rho0 + row) % p.Wq;
+        }
+        if (t2 >= J.nrows && t2 < TILE) {  // padding rows
+          noff[t2] = -INFINITY;
+          rowpos[t2] = -1;
+        }
       }
-      if (t2 < TILE) {
+      if (p.g == 1 && t2 < TILE) {
         const bool rvalid = t2 < J.nrows;
         noff[t2] = (rvalid && Z > 0.f) ? -(M + lg2(Z)) : -INFINITY;
         rowpos[t2] = rvalid ? p.L - p.Wq + (J.rho0 + t2) % p.Wq : -1;

@@ -416,14 +416,21 @@ def run_profile_driver(args):
     decode: four launches of the 32-layer Mistral-shaped decode at n = 1100 on the
             compact caches (the prompt is freed before the launches);
     aux:    two layers of the H2O (OPT-6.7B) shape, prefill + 4 steps, then two layers
-            of the StreamingLLM (Llama-2-13B) shape, fill + 4 steady-state steps."""
+            of the StreamingLLM (Llama-2-13B) shape, fill + 4 steady-state steps;
+    long:   three compressions of two layers of the long-context shape (L = 131072)."""
     import torch
 
     import attention_score_kv_snapkv_gb300 as kvc
     import workloads as WL
 
     dev = torch.device("cuda")
-    if args.profile == "decode":
+    if args.profile == "long":
+        w = WL.LONG
+        x = WL.snapkv_prompt(w, 5, dev, layers=2)
+        for _ in range(3):
+            kvc.snapkv_compress(x["Q_win"], x["K"], x["V"], keep_window=w.window,
+                                pool_kernel=w.pool_kernel, budget=w.budget, cap=w.budget)
+    elif args.profile == "decode":
         w = WL.MISTRAL
         x = WL.snapkv_prompt(w, 5, dev)
         res = kvc.snapkv_compress(x["Q_win"], x["K"], x["V"], keep_window=W, pool_kernel=P,
@@ -685,7 +692,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-aux", action="store_true",
                     help="skip the long-context, H2O and streaming measurements")
-    ap.add_argument("--profile", choices=["decode", "aux"], default=None,
+    ap.add_argument("--profile", choices=["decode", "aux", "long"], default=None,
                     help="run a short fixed workload for an ncu capture instead of the bench")
     ap.add_argument("--layers", type=int, default=32, help="profiling only: fewer layers")
     ap.add_argument("--decode-steps", type=int, default=256, help="profiling only")
