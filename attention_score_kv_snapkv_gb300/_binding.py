@@ -34,7 +34,7 @@ class KVCError(RuntimeError):
 class SnapKVParams(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "n_layers", "batch", "n_q_heads", "n_kv_heads", "head_dim", "prompt_len", "n_query",
-        "keep_window", "pool_kernel", "budget", "cap")]
+        "keep_window", "pool_kernel", "budget", "cap", "pool_avg")]
 
 
 class DecodeParams(ctypes.Structure):
@@ -168,12 +168,13 @@ def kvc_selftest_wait_timeout(timeout_us, stream=None):
     return lib().kvc_selftest_wait_timeout(int(timeout_us), _stream(stream))
 
 
-def snapkv_params(q_win, k, n_query, keep_window, pool_kernel, budget, cap):
+def snapkv_params(q_win, k, n_query, keep_window, pool_kernel, budget, cap, pool_avg=False):
     Ly, B, Hq, Wq, D = q_win.shape
     Ly2, B2, Hkv, L, D2 = k.shape
     if (Ly, B, D) != (Ly2, B2, D2) or Wq != n_query:
         raise ValueError("q_win %s and k %s disagree" % (tuple(q_win.shape), tuple(k.shape)))
-    return SnapKVParams(Ly, B, Hq, Hkv, D, L, n_query, keep_window, pool_kernel, budget, cap)
+    return SnapKVParams(Ly, B, Hq, Hkv, D, L, n_query, keep_window, pool_kernel, budget, cap,
+                        1 if pool_avg else 0)
 
 
 def snapkv_workspace_bytes(params):
@@ -182,10 +183,12 @@ def snapkv_workspace_bytes(params):
 
 def snapkv_compress(q_win, k, v, *, keep_window, pool_kernel, budget, cap=None, k_out=None,
                     v_out=None, pos_out=None, n_valid_out=None, votes_out=None,
-                    kept_scores_out=None, want_votes=False, workspace_buf=None, stream=None):
+                    kept_scores_out=None, want_votes=False, workspace_buf=None, stream=None,
+                    pool_avg=False):
     """SnapKV compression of every (layer, batch, KV head): q_win [Ly,B,Hq,W,D] (the last
     W prompt queries), k, v [Ly,B,Hkv,L,D] -> compact cache [Ly,B,Hkv,cap,D], positions,
-    n_valid (and the raw votes with want_votes).  Returns a dict of the output tensors."""
+    n_valid (and the raw votes with want_votes).  pool_avg selects average pooling instead
+    of max pooling.  Returns a dict of the output tensors."""
     bf = torch.bfloat16
     _need(q_win, "q_win", bf)
     _need(k, "k", bf)
@@ -193,7 +196,7 @@ def snapkv_compress(q_win, k, v, *, keep_window, pool_kernel, budget, cap=None, 
     Ly, B, Hkv, L, D = k.shape
     n_keep = L if (budget >= L or keep_window >= L) else budget
     cap = n_keep if cap is None else cap
-    p = snapkv_params(q_win, k, q_win.shape[3], keep_window, pool_kernel, budget, cap)
+    p = snapkv_params(q_win, k, q_win.shape[3], keep_window, pool_kernel, budget, cap, pool_avg)
     dev = k.device
     if k_out is None:
         k_out = torch.empty((Ly, B, Hkv, cap, D), dtype=bf, device=dev)

@@ -95,7 +95,8 @@ kvc_status plan_snapkv(const kvc_snapkv_params *p, bool want_scores, int num_sms
   if (!common_heads_ok(p->n_layers, p->batch, p->n_q_heads, p->n_kv_heads, p->head_dim))
     return KVC_ERR_SHAPE;
   if (p->prompt_len < 1 || p->n_query < 1 || p->n_query > p->prompt_len || p->keep_window < 0 ||
-      p->pool_kernel < 1 || (p->pool_kernel & 1) == 0 || p->budget < 1 || p->cap < 1)
+      p->pool_kernel < 1 || (p->pool_kernel & 1) == 0 || p->budget < 1 || p->cap < 1 ||
+      (p->pool_avg != 0 && p->pool_avg != 1))
     return KVC_ERR_SHAPE;
   s->units = (long long)p->n_layers * p->batch * p->n_kv_heads;
   s->G = p->n_q_heads / p->n_kv_heads;
@@ -178,6 +179,7 @@ kvc_status run_snapkv(const kvc_snapkv_params *p, const void *q_win, const void 
   sa.D = p->head_dim;
   sa.keep_window = p->keep_window;
   sa.pool_kernel = p->pool_kernel;
+  sa.pool_avg = p->pool_avg;
   sa.budget = p->budget;
   sa.cap = p->cap;
   sa.identity = s.identity ? 1 : 0;
@@ -344,6 +346,7 @@ size_t h2o_prefill_workspace_bytes(const kvc_h2o_params *p, int32_t prompt_len) 
   s.n_query = prompt_len;
   s.keep_window = p->n_recent;
   s.pool_kernel = 1;
+  s.pool_avg = 0;
   s.budget = p->n_heavy + p->n_recent;
   s.cap = p->n_heavy + p->n_recent + 1;
   return snapkv_workspace_bytes(&s);
@@ -368,6 +371,7 @@ kvc_status h2o_prefill(const kvc_h2o_params *p, int32_t prompt_len, const void *
   s.n_query = prompt_len;
   s.keep_window = p->n_recent;
   s.pool_kernel = 1;
+  s.pool_avg = 0;
   s.budget = p->n_heavy + p->n_recent;
   s.cap = p->n_heavy + p->n_recent + 1;
   kvc_status r = run_snapkv(&s, q, k, v, st->k, st->v, st->pos, st->n_used, nullptr, st->score,

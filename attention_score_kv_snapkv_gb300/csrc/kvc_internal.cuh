@@ -355,6 +355,7 @@ struct SelectArgs {
   int32_t *n_valid_out; // [U]
   float *kept_scores;   // [U, cap] or null
   int units, L, D, keep_window, pool_kernel, budget, cap;
+  int pool_avg;         // 1: average pool (window sum / P, zeros past the ends), 0: max
   int identity;         // keep every position (budget >= L or W_keep >= L)
   int32_t *sel_ws;      // [U, cap] scratch for the selected positions
 };

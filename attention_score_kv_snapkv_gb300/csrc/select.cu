@@ -1,10 +1,12 @@
-// SnapKV steps 3-4 (SnapKV article, 処理の流れ steps 3 and 4): 1D max-pool of the vote
-// over the prefix candidates, per-head top-k (equal pooled votes: lower position
-// first), then the gather of the kept prefix rows and the kept window into the compact
-// cache.  The same code cuts H2O's prompt to heavy hitters + recent window (pool 1).
+// SnapKV steps 3-4 (SnapKV article, 処理の流れ steps 3 and 4): 1D pooling of the vote
+// over the prefix candidates (max-pool, or the window average as the pooling variant),
+// per-head top-k (equal pooled votes: lower position first), then the gather of the
+// kept prefix rows and the kept window into the compact cache.  The same code cuts
+// H2O's prompt to heavy hitters + recent window (pool 1).
 //
 // pool_topk_kernel: one CTA (512 threads, two per SM) per unit.
-//   phase 0  pooled vote u_j = max(v[j-h .. j+h]) (cut at the candidate range) turned
+//   phase 0  pooled vote u_j = max(v[j-h .. j+h]) (cut at the candidate range; or the
+//            sum of that window / (2h + 1), zeros past the ends, for average pooling) turned
 //            into an order-preserving uint32 key, kept in shared memory (global
 //            workspace when the candidate range does not fit); the votes are staged
 //            through shared memory in chunks;
@@ -43,6 +45,7 @@ __device__ __forceinline__ uint32_t order_key(float x) {
 struct TopkP {
   const float *votes;  // [U, L]
   int L, n_cand, k, half;  // half = (pool kernel - 1) / 2
+  int avg;             // 1: window average (sum / (2 half + 1), zeros past the ends), 0: max
   int32_t *sel;        // [U, cap] output positions
   int cap;
   uint32_t *kglobal;   // [U, n_cand] keys when they do not fit in shared memory
@@ -73,8 +76,12 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
   const float *v = p.votes + (size_t)u * p.L;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = p.half;
+  const bool avg = p.avg != 0;                  // CTA-uniform
+  const float pad = avg ? 0.f : -INFINITY;      // value beyond both ends of the candidates
+  const float inv = 1.f / (float)(2 * h + 1);
 
-  // phase 0: pooled keys u_j = max(v[j-h .. j+h]) cut at the candidate range.  The
+  // phase 0: pooled keys u_j = max(v[j-h .. j+h]) cut at the candidate range (or the
+  // window average with zero padding).  The
   // votes are staged through shared memory (coalesced, read once from L2): all of them
   // at once into the key array when it is in shared memory (each thread keeps its
   // pooled values in registers until every window has been read), else in chunks.
@@ -91,7 +98,7 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int q = j1 + e * NT - 3;  // position, halo of 3 on both sides
-        t8[e] = (q >= 0 && q < n) ? __ldg(v + q) : -INFINITY;
+        t8[e] = (q >= 0 && q < n) ? __ldg(v + q) : pad;
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -105,12 +112,18 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
 #pragma unroll
     for (int i = 0; i < RUN + 6; ++i) {
       const int jj = j0 + i;  // staged index of position j0 + i - 3
-      w[i] = jj < n + 6 ? vs[jj + (jj >> 5)] : -INFINITY;
+      w[i] = jj < n + 6 ? vs[jj + (jj >> 5)] : pad;
     }
     float mx[RUN];
+    if (avg) {
 #pragma unroll
-    for (int i = 0; i < RUN; ++i)
-      mx[i] = fmax3(fmax3(w[i], w[i + 1], w[i + 2]), fmax3(w[i + 3], w[i + 4], w[i + 5]), w[i + 6]);
+      for (int i = 0; i < RUN; ++i)  // left to right, then the 1/P scale
+        mx[i] = (((((w[i] + w[i + 1]) + w[i + 2]) + w[i + 3]) + w[i + 4]) + w[i + 5] + w[i + 6]) * inv;
+    } else {
+#pragma unroll
+      for (int i = 0; i < RUN; ++i)
+        mx[i] = fmax3(fmax3(w[i], w[i + 1], w[i + 2]), fmax3(w[i + 3], w[i + 4], w[i + 5]), w[i + 6]);
+    }
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < RUN; ++i)
@@ -125,7 +138,7 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int j = lo + i1 + e * NT;
-          t8[e] = (i1 + e * NT < CHUNK && j >= 0 && j < n) ? __ldg(v + j) : -INFINITY;
+          t8[e] = (i1 + e * NT < CHUNK && j >= 0 && j < n) ? __ldg(v + j) : pad;
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e)
@@ -135,7 +148,12 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
       const int cnt = min(step, n - c0);
       for (int i = tid; i < cnt; i += NT) {
         float m = stage[i];
-        for (int t = 1; t <= 2 * h; ++t) m = fmaxf(m, stage[i + t]);
+        if (avg) {
+          for (int t = 1; t <= 2 * h; ++t) m += stage[i + t];
+          m *= inv;
+        } else {
+          for (int t = 1; t <= 2 * h; ++t) m = fmaxf(m, stage[i + t]);
+        }
         kb[kidx(c0 + i)] = order_key(m);
       }
       __syncthreads();
@@ -144,7 +162,12 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
     for (int j = tid; j < n; j += NT) {
       const int lo = max(0, j - h), hi = min(n - 1, j + h);
       float m = v[lo];
-      for (int t = lo + 1; t <= hi; ++t) m = fmaxf(m, v[t]);
+      if (avg) {  // the zeros past the ends add nothing
+        for (int t = lo + 1; t <= hi; ++t) m += v[t];
+        m *= inv;
+      } else {
+        for (int t = lo + 1; t <= hi; ++t) m = fmaxf(m, v[t]);
+      }
       kb[kidx(j)] = order_key(m);
     }
   }
@@ -378,6 +401,7 @@ cudaError_t launch_select_gather(const Ctx &c, const SelectArgs &a) {
     tp.n_cand = n_cand;
     tp.k = k_pick;
     tp.half = (a.pool_kernel - 1) / 2;
+    tp.avg = a.pool_avg;
     tp.sel = a.sel_ws;
     tp.cap = a.cap;
     tp.kglobal = reinterpret_cast<uint32_t *>(a.sel_ws + (size_t)a.units * a.cap);

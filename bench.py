@@ -370,11 +370,71 @@ def measure_h2o(kvc, WL, dev, hbm_peak, steps=64):
             "steps_timed": steps, "device_status": status}
 
 
-def measure_stream(kvc, WL, dev, hbm_peak, steps=256):
+def measure_budget(kvc, Q, K, V, budget, hbm_peak, reps=5):
+    """Compression of the headline prompt at another budget (the cache holds exactly the
+    budget): CUDA-event time per call after two warm-up calls."""
+    import torch
+    Ly, Bb, Hkv, Ll, Dd = K.shape
+    for _ in range(2):
+        res = kvc.snapkv_compress(Q, K, V, keep_window=W, pool_kernel=P, budget=budget, cap=budget)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        kvc.snapkv_compress(Q, K, V, keep_window=W, pool_kernel=P, budget=budget, cap=budget,
+                            k_out=res["k"], v_out=res["v"], pos_out=res["pos"],
+                            n_valid_out=res["n_valid"])
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    per = (Q.shape[2] * W * Dd * 2 + Hkv * Ll * Dd * 2 + 8 * Hkv * (Ll - W)
+           + 8 * Hkv * budget * Dd + 4 * Hkv * budget)
+    byts = Ly * Bb * per
+    status = kvc.kvc_device_status()
+    del res
+    torch.cuda.empty_cache()
+    return {"budget": budget, "compress_ms": ms, "prefix_tokens_per_s": Bb * Ll / (ms / 1e3),
+            "compress_frac_of_hbm_peak": byts / (ms / 1e3) / 1e9 / hbm_peak,
+            "device_status": status}
+
+
+def measure_pool(kvc, Q, K, V, planted, pool_kernel, pool_avg, reps=5):
+    """Pooling ablation on the headline prompt: max-pool, average pool or none (kernel 1).
+    Reports the compression time and the share of the planted hot-span positions that
+    the selection keeps (a synthetic stand-in for the retrieval ablation)."""
+    import torch
+    Ly, Bb, Hkv, Ll, Dd = K.shape
+    kw = dict(keep_window=W, pool_kernel=pool_kernel, budget=KB, cap=KB, pool_avg=pool_avg)
+    res = kvc.snapkv_compress(Q, K, V, **kw)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        kvc.snapkv_compress(Q, K, V, k_out=res["k"], v_out=res["v"], pos_out=res["pos"],
+                            n_valid_out=res["n_valid"], **kw)
+    b.record()
+    torch.cuda.synchronize()
+    kept = torch.zeros((Ly, Bb, Hkv, Ll), dtype=torch.bool, device=K.device)
+    kept.scatter_(3, res["pos"].long().clamp(min=0), True)
+    recall = kept.gather(3, planted).float().mean().item() if planted.numel() else None
+    status = kvc.kvc_device_status()
+    del res, kept
+    torch.cuda.empty_cache()
+    return {"pool": "none" if pool_kernel == 1 else ("avg" if pool_avg else "max"),
+            "pool_kernel": pool_kernel, "compress_ms": a.elapsed_time(b) / reps,
+            "planted_positions_kept": recall, "device_status": status}
+
+
+def measure_stream(kvc, WL, dev, hbm_peak, steps=256, n_sink=None, ring=None):
     """StreamingLLM on Llama-2-13B shapes (batch 16, 40 layers, 40 MHA heads, 4 sinks +
-    2044-token ring): fill the cache, then steady-state steps of append + attention."""
+    2044-token ring, or the given sink count and ring): fill the cache, then steady-state
+    steps of append + attention."""
+    import dataclasses
+
     import torch
     w = WL.STREAM
+    if n_sink is not None:
+        w = dataclasses.replace(w, n_sink=n_sink, ring=ring)
     Ly, Bb, H, Dd, S, R = w.layers, w.batch, w.kv_heads, w.head_dim, w.n_sink, w.ring
     kc = torch.zeros((Ly, Bb, H, S + R, Dd), dtype=torch.bfloat16, device=dev)
     vc = torch.zeros_like(kc)
@@ -406,7 +466,8 @@ def measure_stream(kvc, WL, dev, hbm_peak, steps=256):
     status = kvc.kvc_device_status()
     del kc, vc
     torch.cuda.empty_cache()
-    return {"workload": w.name, "step_ms": ms, "step_GBps": step_bytes / (ms / 1e3) / 1e9,
+    return {"workload": w.name, "n_sink": S, "ring": R, "step_ms": ms,
+            "step_GBps": step_bytes / (ms / 1e3) / 1e9,
             "step_frac_of_hbm_peak": step_bytes / (ms / 1e3) / 1e9 / hbm_peak,
             "steps_timed": steps, "launches_per_step": 2, "device_status": status}
 
@@ -667,12 +728,26 @@ def run_ours(args):
     if e2e is not None:
         line["e2e"] = e2e
     if rank == 0 and not args.no_aux:
-        # the other configurations of the hot path, measured after the headline
+        # the other configurations of the hot path, measured after the headline: first
+        # larger budgets on the same prompt
+        budgets = [measure_budget(kvc, Q, K, V, b, hbm_peak) for b in (1024, 2048, 4096)]
+        pools = [measure_pool(kvc, Q, K, V, x["planted"], pk, avg)
+                 for pk, avg in ((7, False), (7, True), (1, False))]
         del Q, K, V, x, kc, vc, graph
         torch.cuda.empty_cache()
-        line["aux"] = {"long_context": measure_long(kvc, WL, dev, hbm_peak),
+        line["aux"] = {"mistral_budget_sweep": budgets,
+                       "mistral_pool_ablation": pools,
+                       "long_context": measure_long(kvc, WL, dev, hbm_peak),
                        "h2o": measure_h2o(kvc, WL, dev, hbm_peak),
-                       "streaming": measure_stream(kvc, WL, dev, hbm_peak)}
+                       "streaming": measure_stream(kvc, WL, dev, hbm_peak),
+                       # plain window attention (no sinks) and other sink counts, with the
+                       # same 2048-slot cache per head
+                       "streaming_sink_sweep": [
+                           {k2: v2 for k2, v2 in measure_stream(kvc, WL, dev, hbm_peak, steps=64,
+                                                                n_sink=S, ring=2048 - S).items()
+                            if k2 in ("n_sink", "ring", "step_ms", "step_GBps",
+                                      "step_frac_of_hbm_peak", "device_status")}
+                           for S in (0, 1, 2, 4, 8)]}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:

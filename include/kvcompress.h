@@ -101,9 +101,11 @@ typedef struct {
   int32_t n_query;     /* Wq, 1 <= Wq <= L: trailing prompt queries that vote.  SnapKV:
                           the observation window W.  H2O prefill: Wq = L. */
   int32_t keep_window; /* W_keep >= 0: trailing prompt positions always kept (SnapKV: W) */
-  int32_t pool_kernel; /* odd P >= 1: 1D max-pool kernel over the vote (1 = no pooling) */
+  int32_t pool_kernel; /* odd P >= 1: 1D pooling kernel over the vote (1 = no pooling) */
   int32_t budget;      /* Kb: kept entries including the window; W_keep <= Kb */
   int32_t cap;         /* rows per unit of the output cache; cap >= min(Kb, L) */
+  int32_t pool_avg;    /* 0: max-pool (the SnapKV default); 1: average pool, the window's sum
+                          divided by P with zeros beyond both ends of the candidates */
 } kvc_snapkv_params;
 
 /* Bytes of device workspace snapkv_compress needs for *p (0 is never returned). */
@@ -115,7 +117,8 @@ size_t snapkv_workspace_bytes(const kvc_snapkv_params *p);
  *      window keys causally) with scale 1/sqrt(D);
  *   2. vote v_j = sum of those probabilities over the G*Wq rows (fp32);
  *   3. u = 1D max-pool of v over the candidates 0..L-W_keep-1 (kernel P, stride 1,
- *      windows cut at both ends);
+ *      windows cut at both ends), or with pool_avg the window average
+ *      u_j = (1/P) sum_{|t-j| <= (P-1)/2, 0 <= t < L-W_keep} v_t;
  *   4. the k = Kb - W_keep candidates with the largest u (equal u: lower position
  *      first), in ascending position order, followed by the W_keep trailing positions;
  *      their K/V rows are gathered into rows 0..n-1 of the unit's compact cache.

@@ -18,7 +18,8 @@ Readings where the article is silent (each is listed with its reason in DESIGN.m
 softmax over every key a window row may see (prefix plus the causal part of the
 window), scale 1/sqrt(d), plain sum over window rows, selection per KV head with the
 vote summed over the G query heads of the group, max-pool with odd kernel P, stride 1,
-same length, truncated at the ends and run over the prefix candidates only, top-k
+same length, truncated at the ends and run over the prefix candidates only (the
+average-pool variant: window sum over P with zeros past the ends), top-k
 ties resolved towards the lower position, budget counting the window, kept prefix
 positions in ascending order followed by the window, budget >= prompt length keeping
 everything.
@@ -73,6 +74,22 @@ def max_pool_1d(v, kernel):
     return u
 
 
+def avg_pool_1d(v, kernel):
+    """Step 3, the average-pooling variant: u_j = (1/kernel) * sum of v over the positions
+    within (kernel-1)/2 of j, with zeros beyond both ends of ``v`` (the divisor stays the
+    kernel size at the edges).  Stride 1 and same length.
+    """
+    if kernel < 1 or kernel % 2 == 0:
+        raise ValueError("pool kernel must be odd and >= 1")
+    v = np.asarray(v, dtype=np.float64)
+    n = v.shape[0]
+    h = (kernel - 1) // 2
+    u = np.empty(n, dtype=np.float64)
+    for j in range(n):
+        u[j] = v[max(0, j - h): min(n, j + h + 1)].sum() / kernel
+    return u
+
+
 def top_k_lowest_index(u, k):
     """Step 3 top-k: the k positions with the largest u; equal u -> lower position first.
 
@@ -89,9 +106,10 @@ def top_k_lowest_index(u, k):
     return np.sort(order[:k]).astype(np.int64)
 
 
-def select_positions(votes, prompt_len, keep_window, pool_kernel, budget):
+def select_positions(votes, prompt_len, keep_window, pool_kernel, budget, pool="max"):
     """Positions kept for one KV head: pooled top-(budget - keep_window) of the prefix,
-    ascending, followed by the last ``keep_window`` prompt positions (step 4).
+    ascending, followed by the last ``keep_window`` prompt positions (step 4).  ``pool``
+    is "max" (max_pool_1d) or "avg" (avg_pool_1d).
 
     budget >= prompt_len (or keep_window >= prompt_len) keeps every position.
     """
@@ -101,12 +119,21 @@ def select_positions(votes, prompt_len, keep_window, pool_kernel, budget):
     if budget < W:
         raise ValueError("budget smaller than the kept window")
     prefix = np.asarray(votes, dtype=np.float64)[: L - W]
-    pooled = max_pool_1d(prefix, pool_kernel)
+    pooled = pool_1d(prefix, pool_kernel, pool)
     chosen = top_k_lowest_index(pooled, budget - W)
     return np.concatenate([chosen, np.arange(L - W, L, dtype=np.int64)])
 
 
-def compress_unit(q_unit, K, V, window, pool_kernel, budget):
+def pool_1d(v, kernel, pool="max"):
+    """Step 3 with the chosen pooling: "max" or "avg"."""
+    if pool == "max":
+        return max_pool_1d(v, kernel)
+    if pool == "avg":
+        return avg_pool_1d(v, kernel)
+    raise ValueError("pool must be 'max' or 'avg'")
+
+
+def compress_unit(q_unit, K, V, window, pool_kernel, budget, pool="max"):
     """Whole SnapKV compression of one KV head.
 
     Returns (positions [n], K_c [n, d], V_c [n, d], votes [L]) with n = min(budget, L).
@@ -115,11 +142,11 @@ def compress_unit(q_unit, K, V, window, pool_kernel, budget):
     V = np.asarray(V, dtype=np.float64)
     L = K.shape[0]
     votes = window_votes(q_unit, K)
-    pos = select_positions(votes, L, window, pool_kernel, budget)
+    pos = select_positions(votes, L, window, pool_kernel, budget, pool)
     return pos, K[pos], V[pos], votes
 
 
-def compress(Q_win, K, V, window, pool_kernel, budget):
+def compress(Q_win, K, V, window, pool_kernel, budget, pool="max"):
     """SnapKV over a batch: Q_win [B, Hq, W, d], K/V [B, Hkv, L, d].
 
     Query head h belongs to KV head h // (Hq // Hkv).  Returns per-(b, kv-head) lists
@@ -136,6 +163,6 @@ def compress(Q_win, K, V, window, pool_kernel, budget):
         row = []
         for h in range(Hkv):
             row.append(compress_unit(Q_win[b, h * G:(h + 1) * G], K[b, h], V[b, h],
-                                     window, pool_kernel, budget))
+                                     window, pool_kernel, budget, pool))
         out.append(row)
     return out

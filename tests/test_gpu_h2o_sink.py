@@ -148,3 +148,33 @@ def test_sink_ring_tiny_workload(kvc):
     p = pos.cpu().numpy()[0, 0, 0]
     assert list(p[:S]) == list(range(S))
     assert sorted(p[S:]) == list(range(w.stream_len - R, w.stream_len))
+
+
+@pytest.mark.parametrize("n_sink", [0, 1, 2, 8], ids=lambda s: "sinks%d" % s)
+def test_sink_count_sweep_gqa(kvc, n_sink):
+    """Plain window attention (no sinks) and other sink counts: fill, wrap and stream
+    past the ring several times, GQA with two query heads per KV head, every step
+    checked against the oracle's sink + ring cache."""
+    S, R, D, Ly, B, Hkv, G = n_sink, 20, 128, 1, 2, 2, 2
+    T = S + 3 * R + 5
+    dev = torch.device("cuda")
+    kc = torch.zeros((Ly, B, Hkv, S + R, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    pos = torch.full((Ly, B, Hkv, S + R), -1, dtype=torch.int32, device=dev)
+    caches = {(b, h): OSt.SinkCache(S, R, D) for b in range(B) for h in range(Hkv)}
+    g = torch.Generator().manual_seed(100 + n_sink)
+    for t in range(T):
+        q = torch.randn((Ly, B, Hkv * G, D), generator=g).to(torch.bfloat16)
+        k = torch.randn((Ly, B, Hkv, D), generator=g).to(torch.bfloat16)
+        v = torch.randn((Ly, B, Hkv, D), generator=g).to(torch.bfloat16)
+        kvc.sink_window_append(k.to(dev), v.to(dev), kc, vc, t, n_sink=S, n_recent=R, pos=pos)
+        out = kvc.compressed_decode_attn(q.to(dev), kc, vc, n_uniform=min(t + 1, S + R))
+        outh, qh = f64(out), f64(q)
+        for (b, h), c in caches.items():
+            c.append(t, f64(k)[0, b, h], f64(v)[0, b, h])
+            ref = c.attend(qh[0, b, h * G:(h + 1) * G], t)
+            assert_outputs_close(outh[0, b, h * G:(h + 1) * G], ref, "sinks %d step %d" % (S, t))
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    p = pos.cpu().numpy()[0, 1, 1]
+    assert sorted(p.tolist()) == sorted(OSt.visible_positions(T - 1, S, R).tolist())

@@ -128,3 +128,78 @@ def test_argument_errors_launch_nothing(kvc):
     assert e.value.code == 2
     with pytest.raises(TypeError):
         kvc.snapkv_compress(q.float(), k, k, keep_window=8, pool_kernel=3, budget=16)
+
+
+def test_multiple_budgets_same_prompt(kvc):
+    """Budgets 64, 256, 1024 and 2048 on one prompt (GQA-4, D 128, L 4096): every call
+    matches the oracle, and without boundary swaps each smaller budget's picks are a
+    subset of the larger one's (top-k sets nest)."""
+    case = ("budgets-gqa4-L4096", 1, 1, 8, 2, 128, 4096, 32, 7, 64)
+    w, x = make_inputs(case, seed=23)
+    L, Wn, P = w.prompt_len, w.window, w.pool_kernel
+    G = w.q_heads // w.kv_heads
+    dev = torch.device("cuda")
+    Q, K, V = (x[n].to(dev) for n in ("Q_win", "K", "V"))
+    Qh, Kh = f64(x["Q_win"]), f64(x["K"])
+    pooled = [OS.max_pool_1d(OS.window_votes(Qh[0, 0, h * G:(h + 1) * G], Kh[0, 0, h])[:L - Wn], P)
+              for h in range(w.kv_heads)]
+    picks = {}
+    swaps = 0
+    for Kb in (64, 256, 1024, 2048):
+        res = kvc.snapkv_compress(Q, K, V, keep_window=Wn, pool_kernel=P, budget=Kb, cap=Kb)
+        torch.cuda.synchronize()
+        assert kvc.kvc_device_status() == 0
+        pos = res["pos"].cpu().numpy()
+        k = Kb - Wn
+        for h in range(w.kv_heads):
+            got = pos[0, 0, h]
+            assert list(got[k:]) == list(range(L - Wn, L))
+            s = check_selected_set(got[:k], OS.top_k_lowest_index(pooled[h], k), pooled[h], k,
+                                   "budget %d head %d" % (Kb, h))
+            swaps += s
+            picks[(Kb, h)] = (set(got[:k].tolist()), s)
+            idx = torch.as_tensor(got, dtype=torch.long)
+            assert torch.equal(res["k"][0, 0, h].cpu(), x["K"][0, 0, h, idx])
+    assert swaps <= 2
+    for h in range(w.kv_heads):
+        for small, big in ((64, 256), (256, 1024), (1024, 2048)):
+            (a, sa), (b, sb) = picks[(small, h)], picks[(big, h)]
+            if sa == 0 and sb == 0:
+                assert a <= b
+
+
+AVG_CASES = [  # the three pooling paths: kernel 7 in shared memory, chunked, direct
+    ("avg-gqa4-d128-ragged-L1000", 2, 1, 8, 2, 128, 1000, 32, 7, 256),
+    ("avg-gqa8-kernel5-chunked", 1, 1, 8, 1, 128, 700, 24, 5, 100),
+    ("avg-wide-kernel-direct", 1, 1, 2, 2, 64, 5000, 8, 4097, 64),
+    ("avg-long-unit-group-exchange", 1, 1, 4, 1, 128, 8192, 32, 7, 1024),
+]
+
+
+@pytest.mark.parametrize("case", AVG_CASES, ids=[c[0] for c in AVG_CASES])
+def test_snapkv_average_pool_matches_oracle(kvc, case):
+    w, x = make_inputs(case, seed=29)
+    L, Wn, P, Kb = w.prompt_len, w.window, w.pool_kernel, w.budget
+    G = w.q_heads // w.kv_heads
+    dev = torch.device("cuda")
+    Q, K, V = (x[n].to(dev) for n in ("Q_win", "K", "V"))
+    res = kvc.snapkv_compress(Q, K, V, keep_window=Wn, pool_kernel=P, budget=Kb, cap=Kb,
+                              want_votes=True, pool_avg=True)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    Qh, Kh = f64(x["Q_win"]), f64(x["K"])
+    pos = res["pos"].cpu().numpy()
+    k = Kb - Wn
+    swaps = 0
+    for b in range(w.batch):
+        for h in range(w.kv_heads):
+            votes_ref = OS.window_votes(Qh[0, b, h * G:(h + 1) * G], Kh[0, b, h])
+            assert_votes_close(res["votes"][0, b, h].cpu().numpy(), votes_ref)
+            pooled = OS.avg_pool_1d(votes_ref[:L - Wn], P)
+            got = pos[0, b, h]
+            assert list(got[k:]) == list(range(L - Wn, L))
+            swaps += check_selected_set(got[:k], OS.top_k_lowest_index(pooled, k), pooled, k,
+                                        "avg unit (%d,%d)" % (b, h))
+            idx = torch.as_tensor(got, dtype=torch.long)
+            assert torch.equal(res["k"][0, b, h].cpu(), x["K"][0, b, h, idx])
+    assert swaps <= max(1, w.batch * w.kv_heads // 4)

@@ -141,3 +141,38 @@ def test_group_mapping_query_head_to_kv_head():
     assert pos1[0] == 17 and votes1[:L - W].argmax() == 17
     pos0, _, _, votes0 = res[0][0]
     assert votes0[17] < 0.5 * votes1[17]
+
+
+def test_avg_pool_hand_examples():
+    # a single spike spreads evenly over the kernel; at the edges the divisor stays P
+    v = np.array([0, 0, 0, 7, 0, 0, 0, 0, 0], dtype=float)
+    np.testing.assert_allclose(S.avg_pool_1d(v, 3), [0, 0, 7 / 3, 7 / 3, 7 / 3, 0, 0, 0, 0],
+                               rtol=0, atol=1e-15)
+    np.testing.assert_allclose(S.avg_pool_1d(np.ones(5), 3), [2 / 3, 1, 1, 1, 2 / 3],
+                               rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(S.avg_pool_1d(v, 1), v)
+    with pytest.raises(ValueError):
+        S.avg_pool_1d(v, 2)
+
+
+@pytest.mark.parametrize("kernel", [1, 3, 7, 9])
+def test_avg_pool_is_a_same_length_box_convolution(kernel):
+    # zero-padded moving average == numpy's 'same' convolution with a box of 1/P
+    rng = np.random.default_rng(kernel)
+    v = rng.random(40)
+    ref = np.convolve(v, np.full(kernel, 1.0 / kernel), mode="same")
+    np.testing.assert_allclose(S.avg_pool_1d(v, kernel), ref, rtol=1e-14, atol=1e-15)
+
+
+def test_select_positions_with_average_pooling():
+    # 12 candidates + a window of 2, one pick: an isolated spike wins under max pooling,
+    # the centre of a dense cluster under average pooling
+    votes = np.zeros(14)
+    votes[2] = 1.0                       # spike
+    votes[7:10] = [0.6, 0.6, 0.6]        # cluster
+    u = S.avg_pool_1d(votes[:12], 3)
+    assert u[8] == pytest.approx(0.6) and u[2] == pytest.approx(1 / 3) and u[7] == pytest.approx(0.4)
+    assert list(S.select_positions(votes, 14, 2, 3, 3, pool="max")) == [1, 12, 13]
+    assert list(S.select_positions(votes, 14, 2, 3, 3, pool="avg")) == [8, 12, 13]
+    with pytest.raises(ValueError):
+        S.select_positions(votes, 14, 2, 3, 3, pool="median")
