@@ -271,8 +271,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   const int gamma = blockIdx.x / p.g, xg = blockIdx.x - gamma * p.g;
-  // CTAs past the last whole group (when g does not divide the grid) have no jobs
-  const int njobs = (gamma < p.ngroups && gamma < p.jobs) ? (p.jobs - gamma + p.ngroups - 1) / p.ngroups : 0;
+  // Round k gives the groups jobs k*ngroups .. k*ngroups + ngroups - 1, in group order on
+  // even rounds and reversed on odd ones: when the row tiles of a unit differ in size (the
+  // causal prefill of H2O), a group's jobs then mix small and large tiles instead of
+  // repeating the same few row-tile sizes.  CTAs past the last whole group (when g does
+  // not divide the grid) have no jobs.
+  const int full_rounds = p.jobs / p.ngroups, rem = p.jobs - full_rounds * p.ngroups;
+  const int njobs = gamma >= p.ngroups ? 0
+                    : full_rounds + ((full_rounds & 1) ? (p.ngroups - 1 - gamma < rem) : (gamma < rem));
+  auto job_of = [&](int kk) {
+    return kk * p.ngroups + ((kk & 1) ? p.ngroups - 1 - gamma : gamma);
+  };
 
   volatile int *tag = reinterpret_cast<volatile int *>(ctrl + C_TAG);
   if (warp == 0) {
@@ -285,11 +294,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         Job Ja{}, Jb{};
         int na = 0, nb = 0;
         if (k < njobs) {
-          Ja = job_geo(p, gamma + k * p.ngroups, xg);
+          Ja = job_geo(p, job_of(k), xg);
           na = Ja.t1 - Ja.t0;
         }
         if (k >= LAG) {
-          Jb = job_geo(p, gamma + (k - LAG) * p.ngroups, xg);
+          Jb = job_geo(p, job_of(k - LAG), xg);
           nb = Jb.t1 - Jb.t0;
         }
         if (na > 0) {  // Q tile of job k into buffer k % NQ
@@ -344,11 +353,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         Job Ja{}, Jb{};
         int na = 0, nb = 0;
         if (k < njobs) {
-          Ja = job_geo(p, gamma + k * p.ngroups, xg);
+          Ja = job_geo(p, job_of(k), xg);
           na = Ja.t1 - Ja.t0;
         }
         if (k >= LAG) {
-          Jb = job_geo(p, gamma + (k - LAG) * p.ngroups, xg);
+          Jb = job_geo(p, job_of(k - LAG), xg);
           nb = Jb.t1 - Jb.t0;
         }
         // this issuer's job of the round (pass 1: job k, pass 2: job k - LAG), its Q buffer
@@ -414,7 +423,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int it1 = 0;
     bool ok = true;
     for (int k = 0; k < njobs; ++k) {
-      const int j = gamma + k * p.ngroups;
+      const int j = job_of(k);
       const Job J = job_geo(p, j, xg);
       const int n = J.t1 - J.t0;
       const bool rvalid = lrow < J.nrows;
@@ -571,7 +580,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int it2 = 0;
     bool ok = true;
     for (int k = 0; k < njobs; ++k) {
-      const int j = gamma + k * p.ngroups;
+      const int j = job_of(k);
       const Job J = job_geo(p, j, xg);
       const int n = J.t1 - J.t0;
       // statistics of this job -> per-row offsets in shared memory
