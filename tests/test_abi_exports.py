@@ -52,6 +52,10 @@ def test_host_only_calls():
     assert ws % 256 == 0
     bad = B.SnapKVParams(1, 1, 3, 2, 128, 100, 8, 8, 7, 64, 64)  # Hq % Hkv != 0
     assert lib.snapkv_workspace_bytes(ctypes.byref(bad)) == 256
+    avg = B.SnapKVParams(32, 2, 32, 8, 128, 16384, 32, 32, 7, 1024, 1280, 1)  # average pool
+    assert lib.snapkv_workspace_bytes(ctypes.byref(avg)) == ws
+    bad_pool = B.SnapKVParams(32, 2, 32, 8, 128, 16384, 32, 32, 7, 1024, 1280, 2)  # no such mode
+    assert lib.snapkv_workspace_bytes(ctypes.byref(bad_pool)) == 256
     d = B.DecodeParams(32, 2, 32, 8, 128, 1280, 0, 0)
     assert lib.compressed_decode_attn_workspace_bytes(ctypes.byref(d)) >= 512 * 4
 
