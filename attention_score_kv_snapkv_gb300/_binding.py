@@ -131,6 +131,18 @@ def _need(t, name, dtype, shape=None):
     return t
 
 
+def _need_v(t, shape):
+    """v of snapkv_compress: a CUDA tensor, or a page-locked (pinned) CPU tensor whose kept
+    rows the gather reads over the host link."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda and t.is_pinned():
+        if t.dtype != torch.bfloat16:
+            raise TypeError("v must be torch.bfloat16, got %s" % t.dtype)
+        if not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+            raise ValueError("v must be contiguous with shape %s" % (tuple(shape),))
+        return t
+    return _need(t, "v", torch.bfloat16, shape)
+
+
 _ws_cache = {}
 
 
@@ -187,12 +199,13 @@ def snapkv_compress(q_win, k, v, *, keep_window, pool_kernel, budget, cap=None, 
                     pool_avg=False):
     """SnapKV compression of every (layer, batch, KV head): q_win [Ly,B,Hq,W,D] (the last
     W prompt queries), k, v [Ly,B,Hkv,L,D] -> compact cache [Ly,B,Hkv,cap,D], positions,
-    n_valid (and the raw votes with want_votes).  pool_avg selects average pooling instead
-    of max pooling.  Returns a dict of the output tensors."""
+    n_valid (and the raw votes with want_votes).  v may be a pinned CPU tensor (only the
+    kept rows are read, over the host link).  pool_avg selects average pooling instead of
+    max pooling.  Returns a dict of the output tensors."""
     bf = torch.bfloat16
     _need(q_win, "q_win", bf)
     _need(k, "k", bf)
-    _need(v, "v", bf, k.shape)
+    _need_v(v, k.shape)
     Ly, B, Hkv, L, D = k.shape
     n_keep = L if (budget >= L or keep_window >= L) else budget
     cap = n_keep if cap is None else cap

@@ -145,6 +145,18 @@ kvc_status run_snapkv(const kvc_snapkv_params *p, const void *q_win, const void 
   if (!workspace || workspace_bytes < s.total) return KVC_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KVC_ERR_ALIGN;
   if (!g_encode) return KVC_ERR_CUDA;
+  // v may be page-locked host memory mapped for the device: the gather reads it there
+  cudaPointerAttributes va;
+  if (cudaPointerGetAttributes(&va, v) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return KVC_ERR_UNSUPPORTED;
+  }
+  if (va.type == cudaMemoryTypeHost) {
+    if (!va.devicePointer || !aligned16(va.devicePointer)) return KVC_ERR_UNSUPPORTED;
+    v = va.devicePointer;
+  } else if (va.type != cudaMemoryTypeDevice && va.type != cudaMemoryTypeManaged) {
+    return KVC_ERR_UNSUPPORTED;
+  }
 
   uint8_t *w = reinterpret_cast<uint8_t *>(workspace);
   void *wv_ws = w;

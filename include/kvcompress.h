@@ -124,7 +124,11 @@ size_t snapkv_workspace_bytes(const kvc_snapkv_params *p);
  *      their K/V rows are gathered into rows 0..n-1 of the unit's compact cache.
  *   If Kb >= L or W_keep >= L, every position is kept (n = L) and steps 1-3 are skipped
  *   unless kept_scores_out is given.
- * Inputs (dev, bf16): q_win [Ly,B,Hq,Wq,D], k and v [Ly,B,Hkv,L,D].
+ * Inputs (bf16): q_win [Ly,B,Hq,Wq,D] and k [Ly,B,Hkv,L,D] in device memory; v
+ *   [Ly,B,Hkv,L,D] in device memory or in page-locked host memory mapped for the device
+ *   (cudaHostAlloc, cudaHostRegister): v is read only at the kept rows, so a prompt's V
+ *   can stay on the host and only the kept rows cross the host link.  Other host memory
+ *   returns KVC_ERR_UNSUPPORTED.
  * Outputs (dev): k_out, v_out bf16 [Ly,B,Hkv,cap,D] (rows >= n untouched);
  *   pos_out int32 [Ly,B,Hkv,cap] (kept prompt positions in rows 0..n-1, -1 in rows
  *   n..cap-1); n_valid_out int32 [U] (= n);

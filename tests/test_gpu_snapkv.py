@@ -203,3 +203,24 @@ def test_snapkv_average_pool_matches_oracle(kvc, case):
             idx = torch.as_tensor(got, dtype=torch.long)
             assert torch.equal(res["k"][0, b, h].cpu(), x["K"][0, b, h, idx])
     assert swaps <= max(1, w.batch * w.kv_heads // 4)
+
+
+@pytest.mark.parametrize("case", [CASES[1], CASES[5]], ids=["gqa4-d128-ragged", "keep-all"])
+def test_value_rows_from_pinned_host_memory(kvc, case):
+    """V left in page-locked host memory: the gather reads the kept rows over the host
+    link and the compact cache is bit-identical to the one from a device-resident V."""
+    w, x = make_inputs(case, seed=31)
+    L, Wn, P, Kb = w.prompt_len, w.window, w.pool_kernel, w.budget
+    dev = torch.device("cuda")
+    Q, K, V = (x[n].to(dev) for n in ("Q_win", "K", "V"))
+    hV = x["V"].contiguous().pin_memory()
+    kw = dict(keep_window=Wn, pool_kernel=P, budget=Kb)
+    a = kvc.snapkv_compress(Q, K, V, **kw)
+    b = kvc.snapkv_compress(Q, K, hV, **kw)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    for name in ("k", "v", "pos", "n_valid"):
+        assert torch.equal(a[name], b[name]), name
+    # pageable host memory is refused before anything is launched
+    with pytest.raises(Exception):
+        kvc.snapkv_compress(Q, K, x["V"], **kw)
