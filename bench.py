@@ -649,13 +649,31 @@ def run_ours(args):
             sum(t.numel() * t.element_size() for d in hdec for t in d)
         d2h = hout.numel() * hout.element_size() + hnv.numel() * hnv.element_size()
 
+        # the prompt goes over in chunks of layers on a copy stream, and each chunk is
+        # compressed as soon as it has landed, so compression overlaps the next copy
+        copy_stream = torch.cuda.Stream()
+        nch = 4 if LY % 4 == 0 else 1
+        cl = LY // nch
+
         def e2e_step(rec):
             a, b, c = ev(), ev(), ev()
             a.record(stream)
-            dq.copy_(hQ, non_blocking=True)
-            dk.copy_(hK, non_blocking=True)
-            kvc.snapkv_compress(dq, dk, hV, keep_window=W, pool_kernel=P, budget=KB, cap=CAP,
-                                k_out=kc, v_out=vc, pos_out=pos, n_valid_out=nv)
+            copy_stream.wait_stream(stream)
+            landed = []
+            with torch.cuda.stream(copy_stream):
+                for ci in range(nch):
+                    sl = slice(ci * cl, (ci + 1) * cl)
+                    dq[sl].copy_(hQ[sl], non_blocking=True)
+                    dk[sl].copy_(hK[sl], non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(copy_stream)
+                    landed.append(e)
+            for ci in range(nch):
+                sl = slice(ci * cl, (ci + 1) * cl)
+                stream.wait_event(landed[ci])
+                kvc.snapkv_compress(dq[sl], dk[sl], hV[sl], keep_window=W, pool_kernel=P,
+                                    budget=KB, cap=CAP, k_out=kc[sl], v_out=vc[sl],
+                                    pos_out=pos[sl], n_valid_out=nv[sl])
             hnv.copy_(nv, non_blocking=True)
             b.record(stream)
             for s in range(STEPS):
