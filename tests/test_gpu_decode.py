@@ -169,3 +169,30 @@ def test_decode_many_tiles_per_cta(kvc, shape, append):
         torch.cuda.synchronize()
         assert kvc.kvc_device_status() == 0
         assert_outputs_close(f64(out), oracle_decode(q, kc, vc, n0.numpy()))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_decode_every_head_group_and_dim(kvc, D, G):
+    """Every compiled (D, G) instantiation, with enough units that CTAs stream several
+    tiles and units split between CTAs, ragged row counts and the fused append."""
+    Ly, B, Hkv, cap = 1, 4, 16, 777
+    Hq = Hkv * G
+    q, kc, vc = rand_cache(Ly, B, Hq, Hkv, D, cap, seed=D * 10 + G)
+    g = torch.Generator().manual_seed(D + G)
+    n0 = torch.randint(0, cap, (Ly, B, Hkv), generator=g, dtype=torch.int32)
+    n0.view(-1)[:3] = torch.tensor([0, 1, cap - 1], dtype=torch.int32)
+    kn = torch.randn((Ly, B, Hkv, D), generator=g).to(torch.bfloat16)
+    vn = torch.randn((Ly, B, Hkv, D), generator=g).to(torch.bfloat16)
+    dev = torch.device("cuda")
+    kcd, vcd, nd = kc.to(dev), vc.to(dev), n0.to(dev)
+    out = kvc.compressed_decode_attn(q.to(dev), kcd, vcd, n_valid=nd, k_new=kn.to(dev),
+                                     v_new=vn.to(dev))
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    kc2, vc2 = kc.clone(), vc.clone()
+    for idx in np.ndindex(*n0.shape):
+        kc2[idx + (int(n0[idx]),)] = kn[idx]
+        vc2[idx + (int(n0[idx]),)] = vn[idx]
+    assert torch.equal(nd.cpu(), n0 + 1)
+    assert_outputs_close(f64(out), oracle_decode(q, kc2, vc2, (n0 + 1).numpy()))
