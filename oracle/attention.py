@@ -53,3 +53,16 @@ def attend_masked(q, K, V, visible):
     d = q.shape[-1]
     logits = np.where(np.asarray(visible, dtype=bool), K @ q / np.sqrt(d), -np.inf)
     return softmax(logits) @ np.asarray(V, dtype=np.float64)
+
+
+def causal_prefill(Q, K, V):
+    """Prompt self-attention with the causal mask: row i of Q [L, d] attends to the keys
+    and values 0..i.  Returns O [L, d] in fp64 (one row at a time, written out)."""
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    L = Q.shape[0]
+    O = np.empty((L, V.shape[1]), dtype=np.float64)
+    for i in range(L):
+        O[i] = attend(Q[i], K[: i + 1], V[: i + 1])
+    return O

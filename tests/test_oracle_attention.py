@@ -58,3 +58,25 @@ def test_group_attention_is_per_head():
     out = A.attend_group(qs, K, V)
     for g in range(4):
         np.testing.assert_allclose(out[g], A.attend(qs[g], K, V), rtol=1e-15)
+
+
+def test_causal_prefill_closed_forms_and_second_route():
+    rng = np.random.default_rng(5)
+    L, d = 23, 8
+    Q, K, V = rng.standard_normal((3, L, d))
+    O = A.causal_prefill(Q, K, V)
+    # row 0 sees only key 0
+    np.testing.assert_allclose(O[0], V[0], rtol=0, atol=1e-15)
+    # identical keys: uniform weights, so row i is the running mean of V[0..i]
+    Kc = np.tile(K[0], (L, 1))
+    cum = np.cumsum(V, axis=0) / np.arange(1, L + 1)[:, None]
+    np.testing.assert_allclose(A.causal_prefill(Q, Kc, V), cum, rtol=1e-12, atol=1e-13)
+    # keys and values after row i do not reach row i
+    K2, V2 = K.copy(), V.copy()
+    K2[12:] += 5.0
+    V2[12:] -= 3.0
+    np.testing.assert_array_equal(A.causal_prefill(Q, K2, V2)[:12], O[:12])
+    # a second route: full attention with the future masked to -inf
+    for i in (0, 7, L - 1):
+        vis = np.arange(L) <= i
+        np.testing.assert_allclose(O[i], A.attend_masked(Q[i], K, V, vis), rtol=1e-12, atol=1e-14)
