@@ -10,4 +10,4 @@ from ._binding import (  # noqa: F401
     compressed_decode_attn_noalloc,
     h2o_decode_step, h2o_prefill, kvc_device_status, kvc_selftest_wait_timeout,
     kvc_set_wait_timeout_ns, kvc_version, lib, library_path, sink_window_append,
-    snapkv_compress, snapkv_workspace_bytes)
+    snapkv_compress, snapkv_prefill_attention, snapkv_select, snapkv_workspace_bytes)

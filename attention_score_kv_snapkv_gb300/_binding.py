@@ -67,6 +67,10 @@ _SIGS = {
     "snapkv_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(SnapKVParams)]),
     "snapkv_compress": (ctypes.c_int, [ctypes.POINTER(SnapKVParams), _P, _P, _P, _P, _P, _P, _P,
                                        _P, _P, _P, ctypes.c_size_t, _P]),
+    "snapkv_select": (ctypes.c_int, [ctypes.POINTER(SnapKVParams), _P, _P, _P, _P, _P, _P, _P, _P,
+                                     _P, ctypes.c_size_t, _P]),
+    "snapkv_prefill_attention": (ctypes.c_int, [ctypes.POINTER(SnapKVParams), _P, _P, _P, _P, _P,
+                                                _P]),
     "compressed_decode_attn_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(DecodeParams)]),
     "compressed_decode_attn": (ctypes.c_int, [ctypes.POINTER(DecodeParams), _P, _P, _P, _P, _P, _P,
                                               _P, _P, _P, ctypes.c_size_t, _P]),
@@ -244,6 +248,60 @@ def decode_params(q, k_cache, n_uniform=0, new_pos=0):
     if (Ly, B, D) != (Ly2, B2, D2):
         raise ValueError("q %s and cache %s disagree" % (tuple(q.shape), tuple(k_cache.shape)))
     return DecodeParams(Ly, B, Hq, Hkv, D, cap, n_uniform, new_pos)
+
+
+def snapkv_prefill_attention(q, k, v, *, window=None, out=None, votes_out=None, stream=None):
+    """Causal self-attention of the prompt, q [Ly,B,Hq,L,D], k, v [Ly,B,Hkv,L,D] -> out
+    [Ly,B,Hq,L,D]; with window = W also the SnapKV votes of the last W rows, fp32
+    [Ly,B,Hkv,L].  Returns (out, votes or None)."""
+    bf = torch.bfloat16
+    _need(q, "q", bf)
+    _need(k, "k", bf)
+    _need(v, "v", bf, k.shape)
+    Ly, B, Hkv, L, D = k.shape
+    if q.shape[:2] != k.shape[:2] or q.shape[3:] != k.shape[3:] or q.shape[2] % Hkv:
+        raise ValueError("q %s and k %s disagree" % (tuple(q.shape), tuple(k.shape)))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", bf, q.shape)
+    if window is not None and votes_out is None:
+        votes_out = torch.empty((Ly, B, Hkv, L), dtype=torch.float32, device=k.device)
+    if votes_out is not None:
+        _need(votes_out, "votes_out", torch.float32, (Ly, B, Hkv, L))
+    p = SnapKVParams(Ly, B, q.shape[2], Hkv, D, L, window or 1, 0, 1, 1, 1, 0)
+    code = lib().snapkv_prefill_attention(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                          _ptr(votes_out), _stream(stream))
+    _check(code, "snapkv_prefill_attention")
+    return out, votes_out
+
+
+def snapkv_select(votes, k, v, *, keep_window, pool_kernel, budget, cap=None, pool_avg=False,
+                  stream=None):
+    """Steps 3-4 of snapkv_compress (pool, top-k, gather) from given votes [Ly,B,Hkv,L]
+    (e.g. snapkv_prefill_attention's).  Returns the dict snapkv_compress returns, without
+    votes."""
+    bf = torch.bfloat16
+    _need(votes, "votes", torch.float32)
+    _need(k, "k", bf)
+    _need_v(v, k.shape)
+    Ly, B, Hkv, L, D = k.shape
+    _need(votes, "votes", torch.float32, (Ly, B, Hkv, L))
+    n_keep = L if (budget >= L or keep_window >= L) else budget
+    cap = n_keep if cap is None else cap
+    p = SnapKVParams(Ly, B, Hkv, Hkv, D, L, 1, keep_window, pool_kernel, budget, cap,
+                     1 if pool_avg else 0)
+    dev = k.device
+    k_out = torch.empty((Ly, B, Hkv, cap, D), dtype=bf, device=dev)
+    v_out = torch.empty_like(k_out)
+    pos_out = torch.empty((Ly, B, Hkv, cap), dtype=torch.int32, device=dev)
+    n_valid_out = torch.empty((Ly, B, Hkv), dtype=torch.int32, device=dev)
+    nbytes = snapkv_workspace_bytes(p)
+    ws = workspace(nbytes, dev, "snapkv")
+    code = lib().snapkv_select(ctypes.byref(p), _ptr(votes), _ptr(k), _ptr(v), _ptr(k_out),
+                               _ptr(v_out), _ptr(pos_out), _ptr(n_valid_out), None, _ptr(ws),
+                               ws.numel(), _stream(stream))
+    _check(code, "snapkv_select")
+    return {"k": k_out, "v": v_out, "pos": pos_out, "n_valid": n_valid_out}
 
 
 def compressed_decode_attn_workspace_bytes(params):

@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "kvc_internal.cuh"
+#include "prefill.cuh"
 
 namespace kvc {
 
@@ -127,18 +128,21 @@ int sms_for_sizing() {
   return sms > 0 ? sms : 160;
 }
 
+// votes_in: votes computed elsewhere (the prefill attention); then q_win is not read and
+// the window vote does not run.
 kvc_status run_snapkv(const kvc_snapkv_params *p, const void *q_win, const void *k, const void *v,
                       void *k_out, void *v_out, int32_t *pos_out, int32_t *n_valid_out,
                       float *votes_out, float *kept_scores_out, void *workspace,
-                      size_t workspace_bytes, kvc_stream_t stream) {
+                      size_t workspace_bytes, kvc_stream_t stream, const float *votes_in = nullptr) {
   Ctx c;
   kvc_status st = get_ctx(stream, &c);
   if (st != KVC_OK) return st;
   SnapPlan s;
   st = plan_snapkv(p, kept_scores_out != nullptr || votes_out != nullptr, c.num_sms, &s);
   if (st != KVC_OK) return st;
-  if (!q_win || !k || !v || !k_out || !v_out || !pos_out || !n_valid_out) return KVC_ERR_NULL;
-  if (!aligned16(q_win) || !aligned16(k) || !aligned16(v) || !aligned16(k_out) ||
+  if ((!q_win && !votes_in) || !k || !v || !k_out || !v_out || !pos_out || !n_valid_out)
+    return KVC_ERR_NULL;
+  if ((q_win && !aligned16(q_win)) || (votes_in && !aligned4(votes_in)) || !aligned16(k) || !aligned16(v) || !aligned16(k_out) ||
       !aligned16(v_out) || !aligned4(pos_out) || !aligned4(n_valid_out) ||
       (votes_out && !aligned4(votes_out)) || (kept_scores_out && !aligned4(kept_scores_out)))
     return KVC_ERR_ALIGN;
@@ -162,8 +166,15 @@ kvc_status run_snapkv(const kvc_snapkv_params *p, const void *q_win, const void 
   void *wv_ws = w;
   float *votes = votes_out ? votes_out : reinterpret_cast<float *>(w + align256(s.wv_bytes));
   int32_t *sel_ws = reinterpret_cast<int32_t *>(w + align256(s.wv_bytes) + s.votes_bytes);
+  if (votes_in) {
+    if (votes_out && votes_out != votes_in)
+      if (cudaMemcpyAsync(votes_out, votes_in, (size_t)s.units * p->prompt_len * sizeof(float),
+                          cudaMemcpyDeviceToDevice, c.stream) != cudaSuccess)
+        return KVC_ERR_CUDA;
+    votes = const_cast<float *>(votes_in);
+  }
 
-  if (s.need_votes) {
+  if (s.need_votes && !votes_in) {
     WindowVoteArgs a;
     a.q = q_win;
     a.k = k;
@@ -287,6 +298,48 @@ kvc_status snapkv_compress(const kvc_snapkv_params *p, const void *q_win, const 
   ensure_encode();
   return run_snapkv(p, q_win, k, v, k_out, v_out, pos_out, n_valid_out, votes_out,
                     kept_scores_out, workspace, workspace_bytes, stream);
+}
+
+kvc_status snapkv_select(const kvc_snapkv_params *p, const float *votes, const void *k,
+                         const void *v, void *k_out, void *v_out, int32_t *pos_out,
+                         int32_t *n_valid_out, float *kept_scores_out, void *workspace,
+                         size_t workspace_bytes, kvc_stream_t stream) {
+  ensure_encode();
+  if (!votes) return KVC_ERR_NULL;
+  return run_snapkv(p, nullptr, k, v, k_out, v_out, pos_out, n_valid_out, nullptr,
+                    kept_scores_out, workspace, workspace_bytes, stream, votes);
+}
+
+kvc_status snapkv_prefill_attention(const kvc_snapkv_params *p, const void *q, const void *k,
+                                    const void *v, void *o_out, float *votes_out,
+                                    kvc_stream_t stream) {
+  ensure_encode();
+  Ctx c;
+  kvc_status st = get_ctx(stream, &c);
+  if (st != KVC_OK) return st;
+  if (!p) return KVC_ERR_NULL;
+  if (!common_heads_ok(p->n_layers, p->batch, p->n_q_heads, p->n_kv_heads, p->head_dim) ||
+      p->prompt_len < 1 || (votes_out && (p->n_query < 1 || p->n_query > p->prompt_len)))
+    return KVC_ERR_SHAPE;
+  const long long uq = (long long)p->n_layers * p->batch * p->n_q_heads;
+  if (uq * p->prompt_len > kMaxRows) return KVC_ERR_SHAPE;
+  if (!q || !k || !v || !o_out) return KVC_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_out) ||
+      (votes_out && !aligned4(votes_out)))
+    return KVC_ERR_ALIGN;
+  if (!g_encode) return KVC_ERR_CUDA;
+  PrefillArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o_out;
+  a.votes = votes_out;
+  a.units_q = (int)uq;
+  a.G = p->n_q_heads / p->n_kv_heads;
+  a.L = p->prompt_len;
+  a.D = p->head_dim;
+  a.Wq = p->n_query;
+  return cuda_status(launch_prefill(c, a));
 }
 
 size_t compressed_decode_attn_workspace_bytes(const kvc_decode_params *p) {

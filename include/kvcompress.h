@@ -144,6 +144,34 @@ kvc_status snapkv_compress(const kvc_snapkv_params *p, const void *q_win, const 
                            int32_t *n_valid_out, float *votes_out, float *kept_scores_out,
                            void *workspace, size_t workspace_bytes, kvc_stream_t stream);
 
+/* Steps 3-4 of snapkv_compress from votes computed elsewhere (snapkv_prefill_attention):
+ * pooling, top-k and the gather exactly as snapkv_compress does them, without its window
+ * vote.  votes: dev fp32 [Ly,B,Hkv,L] (read only).  The other arguments, the workspace
+ * (snapkv_workspace_bytes(p) bytes suffice) and the errors are those of snapkv_compress;
+ * p->n_query is not used. */
+kvc_status snapkv_select(const kvc_snapkv_params *p, const float *votes, const void *k,
+                         const void *v, void *k_out, void *v_out, int32_t *pos_out,
+                         int32_t *n_valid_out, float *kept_scores_out, void *workspace,
+                         size_t workspace_bytes, kvc_stream_t stream);
+
+/* The prompt's self-attention with the SnapKV votes as a by-product (SnapKV article,
+ * 推論方法: the compression follows the prompt's processing).  For every (layer, batch,
+ * query head h): o = softmax(q . k^T / sqrt(D)) . v over the prompt with the causal mask
+ * (row i sees positions 0..i; KV head h / G).  With votes_out, the last n_query rows of
+ * every query head also add their probabilities per key into votes_out of their KV head:
+ * the same votes as snapkv_compress's step 2 (fp32; summed over the G heads with atomic
+ * adds, so the order of the additions, and the last bits, can vary between calls).
+ * The query tiles that hold window rows are swept twice (row statistics, then output and
+ * votes); every other tile once.
+ * Uses n_layers, batch, n_q_heads, n_kv_heads, head_dim, prompt_len and n_query of p.
+ * Inputs (dev, bf16): q [Ly,B,Hq,L,D], k, v [Ly,B,Hkv,L,D].  Outputs (dev): o_out bf16
+ * [Ly,B,Hq,L,D]; votes_out fp32 [Ly,B,Hkv,L] or NULL (then n_query is not used).
+ * Needs no workspace.  Errors: KVC_ERR_NULL, KVC_ERR_SHAPE, KVC_ERR_ALIGN, KVC_ERR_CUDA,
+ * KVC_ERR_UNSUPPORTED. */
+kvc_status snapkv_prefill_attention(const kvc_snapkv_params *p, const void *q, const void *k,
+                                    const void *v, void *o_out, float *votes_out,
+                                    kvc_stream_t stream);
+
 /* ------------------------------------------------------------------------------ */
 /* Decode attention over a compact (SnapKV) or ring (StreamingLLM) cache           */
 /* ([SnapKV] 推論方法: decoding reads only the compressed cache; [StreamingLLM]       */
