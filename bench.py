@@ -481,6 +481,53 @@ def measure_pool(kvc, Q, K, V, planted, pool_kernel, pool_avg, reps=5):
             "planted_positions_kept": recall, "device_status": status}
 
 
+def measure_prefill(kvc, WL, dev, tf_peak, layers=2, reps=3):
+    """Prompt self-attention with the votes as a by-product, on `layers` layers of the
+    Mistral-7B-shaped prompt (full 16384-token causal attention): the plain prefill, the
+    prefill with votes, selection from those votes, and the alternative of the plain
+    prefill followed by snapkv_compress."""
+    import torch
+    w = WL.MISTRAL
+    x = WL.snapkv_prompt(w, WL.seed_of(2, 7), dev, layers=layers, full_queries=True)
+    Qf, K, V, Qw = x["Q_full"], x["K"], x["V"], x["Q_win"]
+    out = torch.empty_like(Qf)
+    votes = torch.empty((layers, w.batch, w.kv_heads, w.prompt_len), dtype=torch.float32, device=dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    kw = dict(keep_window=w.window, pool_kernel=w.pool_kernel, budget=w.budget, cap=w.budget)
+    t_plain = timed(lambda: kvc.snapkv_prefill_attention(Qf, K, V, out=out))
+    t_votes = timed(lambda: kvc.snapkv_prefill_attention(Qf, K, V, window=w.window, out=out,
+                                                         votes_out=votes))
+    t_select = timed(lambda: kvc.snapkv_select(votes, K, V, **kw))
+    t_compress = timed(lambda: kvc.snapkv_compress(Qw, K, V, **kw))
+    status = kvc.kvc_device_status()
+    # causal attention work: Q.K^T and P.V over the lower triangle (incl. diagonal)
+    L = w.prompt_len
+    flop = layers * w.batch * w.q_heads * 2 * 2 * w.head_dim * (L * (L + 1) / 2)
+    del x, Qf, K, V, Qw, out, votes
+    torch.cuda.empty_cache()
+    return {"workload": "mistral7b-b2-L16384-gqa32x8-d128, %d layers" % layers,
+            "prefill_ms_per_layer": t_plain / layers,
+            "prefill_TFLOPs": flop / (t_plain / 1e3) / 1e12,
+            "prefill_frac_of_bf16_peak": flop / (t_plain / 1e3) / 1e12 / tf_peak,
+            "prefill_with_votes_ms_per_layer": t_votes / layers,
+            "select_from_votes_ms_per_layer": t_select / layers,
+            "separate_compress_ms_per_layer": t_compress / layers,
+            "fused_path_ms_per_layer": (t_votes + t_select) / layers,
+            "unfused_path_ms_per_layer": (t_plain + t_compress) / layers,
+            "device_status": status}
+
+
 def measure_stream(kvc, WL, dev, hbm_peak, steps=256, n_sink=None, ring=None):
     """StreamingLLM on Llama-2-13B shapes (batch 16, 40 layers, 40 MHA heads, 4 sinks +
     2044-token ring, or the given sink count and ring): fill the cache, then steady-state
@@ -814,6 +861,7 @@ def run_ours(args):
         line["aux"] = {"mistral_budget_sweep": budgets,
                        "mistral_pool_ablation": pools,
                        "long_context": measure_long(kvc, WL, dev, hbm_peak),
+                       "prefill_with_votes": measure_prefill(kvc, WL, dev, tf_peak),
                        "h2o": measure_h2o(kvc, WL, dev, hbm_peak),
                        "streaming": measure_stream(kvc, WL, dev, hbm_peak),
                        # plain window attention (no sinks) and other sink counts, with the
