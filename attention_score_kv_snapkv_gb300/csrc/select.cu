@@ -7,16 +7,17 @@
 // pool_topk_kernel: one CTA (512 threads, two per SM) per unit.
 //   phase 0  pooled vote u_j = max(v[j-h .. j+h]) (cut at the candidate range; or the
 //            sum of that window / (2h + 1), zeros past the ends, for average pooling) turned
-//            into an order-preserving uint32 key, kept in shared memory (global
-//            workspace when the candidate range does not fit); the votes are staged
-//            through shared memory in chunks;
-//   phase 1  radix select of the k-th largest key: four histogram passes over 8-bit
-//            digits, each narrowing the bucket that holds it; every warp counts into
-//            its own histogram, so the few hot bins of the top digit are not contended
-//            across warps;
+//            into an order-preserving uint32 key; the votes are staged through shared
+//            memory (16-byte loads where the row is aligned);
+//   phase 1  radix select of the k-th largest key;
 //   phase 2  stream compaction in position order: keys above the threshold, and the
 //            first `need` keys equal to it (exact lower-position tie rule), written as
 //            ascending positions (per-thread runs, one block-wide scan).
+//   Pool kernel 7 with at most 32 candidates per thread (the usual SnapKV setting) keeps
+//   each thread's 32 keys in registers and selects with three digits (11, 11, 10 bits)
+//   over one shared histogram; other pool sizes and longer prompts keep the keys in
+//   shared (else global) memory and select with four 8-bit digits over per-warp
+//   histograms.
 // gather_kernel: 16-byte vectorised copy of the kept K/V rows, positions, scores.
 #include "kvc_internal.cuh"
 
@@ -65,7 +66,60 @@ __host__ __device__ constexpr int kidx(int j) { return j + (j >> 5); }
 // halo of 3 on both sides
 __host__ __device__ constexpr int key_words(int n) { return n + 6 + (n + 6) / 32 + 1; }
 
+// Fast path (pool kernel 7, candidates fit one run of RUN per thread): the keys stay in
+// registers and the radix select uses three digits (bits 31-21, 20-10, 9-0) over one
+// shared histogram of NB bins.  misc words used: [0] bin found, [1] keys still to take
+// from it, [8, 8 + NWARP) warp totals of the bin search, [32, 32 + NWARP) warp totals of
+// the compaction scan.
+constexpr int NB = 2048;
+constexpr int M_BIN = 0, M_NEED = 1, M_WSUM = 8, M_CSUM = 32;
+static_assert(NWARP * NBIN >= NB, "the fast path's histogram aliases the per-warp histograms");
+
+// Bin search over a histogram of PER * NT bins: finds the bin b holding the need-th largest
+// key (the bins above b hold fewer than `need` keys, b and those above at least `need`;
+// 1 <= need <= the histogram's total) and writes misc[M_BIN] = b, misc[M_NEED] = need minus
+// the keys above b.  Thread t owns bins [t PER, (t + 1) PER); suffix sums run over the
+// lanes of a warp, then over the warps.  Ends synchronised.
+template <int PER>
+__device__ __forceinline__ void find_bin(const uint32_t *hist, int *misc, int need) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t own[PER], s = 0;
+#pragma unroll
+  for (int b = 0; b < PER; ++b) {
+    own[b] = hist[tid * PER + b];
+    s += own[b];
+  }
+  uint32_t incl = s;  // keys in the bins of this lane and every higher lane of the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_down_sync(0xffffffffu, incl, o);
+    if (lane + o < 32) incl += t;
+  }
+  if (lane == 0) misc[M_WSUM + warp] = (int)incl;
+  __syncthreads();
+  uint32_t above = incl - s;
+  for (int w = warp + 1; w < NWARP; ++w) above += (uint32_t)misc[M_WSUM + w];
+  if (above < (uint32_t)need && (uint32_t)need <= above + s) {
+    uint32_t acc = above;
+#pragma unroll
+    for (int b = PER - 1; b >= 0; --b) {
+      if (acc + own[b] >= (uint32_t)need) {
+        misc[M_BIN] = tid * PER + b;
+        misc[M_NEED] = need - (int)acc;
+        break;
+      }
+      acc += own[b];
+    }
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
+  // Programmatic dependent launch: the gather kernel may start launching (its CTAs take
+  // SM slots as these exit, and wait until this grid has completed); this grid waits for
+  // the kernel that wrote the votes.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ uint32_t sm[];
   uint32_t *tot = sm + SM_TOT;
   int *misc = reinterpret_cast<int *>(sm + SM_MISC);  // [0] prefix, [1] need, [2..] warp eq, [2+NWARP..] warp gt
@@ -89,46 +143,154 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
     // pool kernel 7, one run of 32 consecutive positions per thread: the votes go to
     // shared memory with one pad word per 32 (a thread's run is then conflict-free
     // across the warp); the run and its halo are read into registers and the window
-    // maxima formed there (three-input max), then written back as keys in place.
+    // maxima (or sums) formed there.  Staged index jj holds position jj - 3.
     float *vs = reinterpret_cast<float *>(kb);
-    // eight loads in flight per thread before the stores (a plain loop would wait out
-    // the memory latency once per element)
-    for (int j1 = tid; j1 < n + 6; j1 += 8 * NT) {
-      float t8[8];
+    if ((reinterpret_cast<uintptr_t>(v) & 15u) == 0) {
+      // 16-byte loads, all of a thread's in flight together
+      const int n4 = n >> 2;
+      const float4 *v4 = reinterpret_cast<const float4 *>(v);
+      for (int i1 = tid; i1 < n4; i1 += 8 * NT) {
+        float4 t8[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int q = j1 + e * NT - 3;  // position, halo of 3 on both sides
-        t8[e] = (q >= 0 && q < n) ? __ldg(v + q) : pad;
+        for (int e = 0; e < 8; ++e) {
+          const int i = i1 + e * NT;
+          t8[e] = i < n4 ? __ldg(v4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int i = i1 + e * NT;
+          if (i < n4) {
+            const int jj = 4 * i + 3;
+            vs[kidx(jj)] = t8[e].x;
+            vs[kidx(jj + 1)] = t8[e].y;
+            vs[kidx(jj + 2)] = t8[e].z;
+            vs[kidx(jj + 3)] = t8[e].w;
+          }
+        }
       }
+      if (tid < 3) {  // the halo
+        vs[kidx(tid)] = pad;
+        vs[kidx(n + 3 + tid)] = pad;
+      } else if (tid < 3 + (n & 3)) {  // the last n % 4 candidates
+        const int q = (n & ~3) + tid - 3;
+        vs[kidx(q + 3)] = __ldg(v + q);
+      }
+    } else {
+      // eight loads in flight per thread before the stores
+      for (int j1 = tid; j1 < n + 6; j1 += 8 * NT) {
+        float t8[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int j = j1 + e * NT;
-        if (j < n + 6) vs[j + (j >> 5)] = t8[e];
+        for (int e = 0; e < 8; ++e) {
+          const int q = j1 + e * NT - 3;
+          t8[e] = (q >= 0 && q < n) ? __ldg(v + q) : pad;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = j1 + e * NT;
+          if (j < n + 6) vs[kidx(j)] = t8[e];
+        }
       }
     }
+    uint32_t *hist = sm + SM_HIST;
+    for (int b = tid; b < NB; b += NT) hist[b] = 0;
     __syncthreads();
     const int j0 = tid * RUN;
-    float w[RUN + 6];
+    uint32_t key[RUN];  // this thread's pooled keys (positions j0 ..), 0 past the candidates
+    {
+      float w[RUN + 6];
 #pragma unroll
-    for (int i = 0; i < RUN + 6; ++i) {
-      const int jj = j0 + i;  // staged index of position j0 + i - 3
-      w[i] = jj < n + 6 ? vs[jj + (jj >> 5)] : pad;
+      for (int i = 0; i < RUN + 6; ++i) {
+        const int jj = j0 + i;  // staged index of position j0 + i - 3
+        w[i] = jj < n + 6 ? vs[kidx(jj)] : pad;
+      }
+#pragma unroll
+      for (int i = 0; i < RUN; ++i) {
+        const float m = avg ? (((((w[i] + w[i + 1]) + w[i + 2]) + w[i + 3]) + w[i + 4]) + w[i + 5] + w[i + 6]) * inv
+                            : fmax3(fmax3(w[i], w[i + 1], w[i + 2]), fmax3(w[i + 3], w[i + 4], w[i + 5]), w[i + 6]);
+        key[i] = j0 + i < n ? order_key(m) : 0u;
+      }
     }
-    float mx[RUN];
-    if (avg) {
+    // radix pass 0 (bits 31-21): neighbouring pooled values mostly share their top digit,
+    // so a thread adds each run of equal digits with one shared atomic
+    {
+      uint32_t cur = 0xffffffffu, cnt = 0;
 #pragma unroll
-      for (int i = 0; i < RUN; ++i)  // left to right, then the 1/P scale
-        mx[i] = (((((w[i] + w[i + 1]) + w[i + 2]) + w[i + 3]) + w[i + 4]) + w[i + 5] + w[i + 6]) * inv;
-    } else {
-#pragma unroll
-      for (int i = 0; i < RUN; ++i)
-        mx[i] = fmax3(fmax3(w[i], w[i + 1], w[i + 2]), fmax3(w[i + 3], w[i + 4], w[i + 5]), w[i + 6]);
+      for (int i = 0; i < RUN; ++i) {
+        if (j0 + i < n) {
+          const uint32_t b = key[i] >> 21;
+          if (b != cur) {
+            if (cnt) atomicAdd(&hist[cur], cnt);
+            cur = b;
+            cnt = 0;
+          }
+          ++cnt;
+        }
+      }
+      if (cnt) atomicAdd(&hist[cur], cnt);
     }
     __syncthreads();
+    find_bin<NB / NT>(hist, misc, p.k);
+    const uint32_t b0 = (uint32_t)misc[M_BIN];
+    int need = misc[M_NEED];
+#pragma unroll
+    for (int b = 0; b < NB / NT; ++b) hist[tid * (NB / NT) + b] = 0;  // own bins (read above)
+    __syncthreads();
+    // radix pass 1 (bits 20-10) over the keys of bucket b0
 #pragma unroll
     for (int i = 0; i < RUN; ++i)
-      if (j0 + i < n) kb[kidx(j0 + i)] = order_key(mx[i]);
-  } else if (2 * h < CHUNK / 2) {
+      if (j0 + i < n && (key[i] >> 21) == b0) atomicAdd(&hist[(key[i] >> 10) & (NB - 1)], 1u);
+    __syncthreads();
+    find_bin<NB / NT>(hist, misc, need);
+    const uint32_t pre = (b0 << 11) | (uint32_t)misc[M_BIN];  // key >> 10 of the bucket
+    need = misc[M_NEED];
+#pragma unroll
+    for (int b = 0; b < NB / NT; ++b) hist[tid * (NB / NT) + b] = 0;
+    __syncthreads();
+    // radix pass 2 (bits 9-0)
+#pragma unroll
+    for (int i = 0; i < RUN; ++i)
+      if (j0 + i < n && (key[i] >> 10) == pre) atomicAdd(&hist[key[i] & 1023u], 1u);
+    __syncthreads();
+    find_bin<1024 / NT>(hist, misc, need);
+    const uint32_t T = (pre << 10) | (uint32_t)misc[M_BIN];
+    need = misc[M_NEED];
+    // compaction in position order: counts above / equal to the threshold, a block-wide
+    // exclusive scan, then each thread writes its chosen positions (ties: the first
+    // `need` equal keys by position)
+    int gt = 0, eq = 0;
+#pragma unroll
+    for (int i = 0; i < RUN; ++i) {
+      gt += (j0 + i < n && key[i] > T) ? 1 : 0;
+      eq += (j0 + i < n && key[i] == T) ? 1 : 0;
+    }
+    const int packed = gt | (eq << 16);
+    int incl = packed;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) misc[M_CSUM + warp] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w2 = 0; w2 < warp; ++w2) wbase += misc[M_CSUM + w2];
+    const int excl = wbase + incl - packed;
+    int eq_before = excl >> 16;
+    if (gt + eq > 0) {
+      int out = (excl & 0xffff) + min(eq_before, need);
+      int32_t *sel = p.sel + (size_t)u * p.cap;
+#pragma unroll
+      for (int i = 0; i < RUN; ++i) {
+        const bool take = j0 + i < n && (key[i] > T || (key[i] == T && eq_before++ < need));
+        if (take) {
+          if (out < p.k) sel[out] = j0 + i;
+          ++out;
+        }
+      }
+    }
+    return;
+  }
+  if (2 * h < CHUNK / 2) {
     float *stage = reinterpret_cast<float *>(sm + SM_HIST);
     const int step = CHUNK - 2 * h;
     for (int c0 = 0; c0 < n; c0 += step) {
@@ -332,6 +494,8 @@ struct GatherP {
 
 // grid (ceil(cap / 32), U); 256 threads; each CTA fills 32 rows of one unit.
 __global__ void __launch_bounds__(256) gather_kernel(const GatherP p) {
+  // programmatic dependent launch: wait for the kernel that wrote the positions / votes
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int u = blockIdx.y;
   const int r0 = blockIdx.x * 32;
   __shared__ int spos[32];
@@ -405,8 +569,17 @@ cudaError_t launch_select_gather(const Ctx &c, const SelectArgs &a) {
     tp.sel = a.sel_ws;
     tp.cap = a.cap;
     tp.kglobal = reinterpret_cast<uint32_t *>(a.sel_ws + (size_t)a.units * a.cap);
-    pool_topk_kernel<<<a.units, NT, smem, c.stream>>>(tp);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.units);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, pool_topk_kernel, tp);
     if (e != cudaSuccess) return e;
   }
   GatherP gp;
@@ -427,9 +600,16 @@ cudaError_t launch_select_gather(const Ctx &c, const SelectArgs &a) {
   gp.identity = a.identity;
   gp.row_vecs = a.D / 8;
   gp.status = c.status;
-  dim3 grid((a.cap + 31) / 32, a.units);
-  gather_kernel<<<grid, 256, 0, c.stream>>>(gp);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((a.cap + 31) / 32), (unsigned)a.units);
+  cfg.blockDim = dim3(256);
+  cfg.stream = c.stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gather_kernel, gp);
 }
 
 }  // namespace kvc

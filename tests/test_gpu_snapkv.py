@@ -25,6 +25,10 @@ CASES = [
     ("window-is-whole-prompt", 1, 1, 2, 2, 64, 6, 6, 7, 4),
     ("long-unit-group-exchange", 1, 1, 4, 1, 128, 8192, 32, 7, 1024),
     ("tiny-prompt-one-tile", 1, 1, 4, 2, 128, 40, 8, 3, 20),
+    # pool 7 with the keys in registers: 16-byte vote loads plus a tail of n % 4 = 2, and
+    # an odd prompt length whose vote rows are mostly misaligned (4-byte loads)
+    ("window30-vector-tail", 1, 1, 8, 2, 128, 1000, 30, 7, 200),
+    ("odd-length-L1023", 1, 1, 4, 4, 64, 1023, 16, 7, 128),
 ]
 
 
@@ -173,6 +177,7 @@ AVG_CASES = [  # the three pooling paths: kernel 7 in shared memory, chunked, di
     ("avg-gqa8-kernel5-chunked", 1, 1, 8, 1, 128, 700, 24, 5, 100),
     ("avg-wide-kernel-direct", 1, 1, 2, 2, 64, 5000, 8, 4097, 64),
     ("avg-long-unit-group-exchange", 1, 1, 4, 1, 128, 8192, 32, 7, 1024),
+    ("avg-odd-length-L1023", 1, 1, 4, 4, 64, 1023, 16, 7, 128),
 ]
 
 
