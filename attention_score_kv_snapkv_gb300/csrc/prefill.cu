@@ -138,6 +138,60 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
   return x[0];
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of s[0..127]: eight independent chains of three-input max, then a short tree.
+__device__ __forceinline__ float max128(const float *s) {
+  float m[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m[j] = fmax3(s[j], s[j + 8], s[j + 16]);
+#pragma unroll
+  for (int t = 3; t < 15; t += 2)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m[j] = fmax3(m[j], s[j + 8 * t], s[j + 8 * t + 8]);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m[j] = fmaxf(m[j], s[j + 120]);
+  return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
+// Sum of exp2(s[i] c + nm) over i < 128 (c and nm packed twice), four packed chains.
+__device__ __forceinline__ float exp2_sum128(const float *s, unsigned long long cc,
+                                             unsigned long long nm) {
+  unsigned long long a[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int i = 0; i < 128; i += 8) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 x = upk(fma2(pk(s[i + 2 * j], s[i + 2 * j + 1]), cc, nm));
+      a[j] = add2(a[j], pk(ex2(x.x), ex2(x.y)));
+    }
+  }
+  const float2 t = upk(add2(add2(a[0], a[1]), add2(a[2], a[3])));
+  return t.x + t.y;
+}
+
+// s[i] <- exp2(s[i] c + nm) for i < 128; returns their sum (four packed chains).
+__device__ __forceinline__ float exp2_inplace128(float *s, unsigned long long cc,
+                                                 unsigned long long nm) {
+  unsigned long long a[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int i = 0; i < 128; i += 8) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 x = upk(fma2(pk(s[i + 2 * j], s[i + 2 * j + 1]), cc, nm));
+      s[i + 2 * j] = ex2(x.x);
+      s[i + 2 * j + 1] = ex2(x.y);
+      a[j] = add2(a[j], pk(s[i + 2 * j], s[i + 2 * j + 1]));
+    }
+  }
+  const float2 t = upk(add2(add2(a[0], a[1]), add2(a[2], a[3])));
+  return t.x + t.y;
+}
+
 template <int D>
 __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__ CUtensorMap tq,
                                                          const __grid_constant__ CUtensorMap tk,
@@ -299,10 +353,15 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
     }
   } else {
     // ---------------- softmax warps: one query row per thread ----------------
+    // A tile's 128 scores of the row are loaded into registers at once (the score
+    // buffer is released right away), the row max comes from a three-input max tree,
+    // the exponentials are formed before waiting for the previous P.V (only the bf16
+    // stores of P wait for it), and FFMA / FADD run packed two lanes at a time.
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     uint8_t *ptile = smem + Gm::OFF_P;
+    const unsigned long long cc = pk(p.c, p.c);
     int sc = 0, pc = 0;
     bool ok = true;
     for (int k = 0; k < njobs; ++k) {
@@ -310,14 +369,26 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
       const int row = J.qt * ROWS + r;  // position in the prompt
       const bool valid = row < p.L;
       const int ukv = J.uq / p.G;
-      // scores of tile kt (buffer sbf) for this row, 32 columns at a time, masked
-      auto load_chunk = [&](int sbf, int kt, int ch, float (&s)[32]) {
-        tmem_ld32(tmem + lane_base + (uint32_t)(sbf * 128 + ch * 32), s);
-        tmem_wait_ld();
-        const int key0 = kt * KT + ch * 32;
+      // Scores of tile kt (buffer sbf) into s[0..127], the buffer then released.  Only
+      // the diagonal tile (kt == qt) holds keys after the row; rows past the prompt
+      // (the last query tile) keep finite scores of zero-filled queries and never reach
+      // the output or the votes.
+      auto release = [&](int sbf) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar + B_SEMPTY + 8 * sbf);
+      };
+      auto load_tile = [&](int sbf, int kt, float (&sv)[KT], bool rel) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (!valid || key0 + i > row) s[i] = -INFINITY;
+        for (int ch = 0; ch < KT / 32; ++ch)
+          tmem_ld32(tmem + lane_base + (uint32_t)(sbf * 128 + ch * 32), sv + ch * 32);
+        tmem_wait_ld();
+        if (rel) release(sbf);
+        if (kt == J.qt) {
+#pragma unroll
+          for (int i = 0; i < KT; ++i)
+            if (kt * KT + i > row) sv[i] = -INFINITY;
+        }
       };
       float m = -INFINITY, l = 0.f;
       if (J.twice) {  // statistics sweep: exact max and normaliser of every row
@@ -326,32 +397,15 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
           ok = __all_sync(0xffffffffu, ok && ab.wait(bar + B_SFULL + 8 * sbf, (sc >> 1) & 1));
           if (!ok) continue;
           tc_fence_after();
-          float s[32];
-          float tmax = -INFINITY;
-#pragma unroll 1
-          for (int ch = 0; ch < KT / 32; ++ch) {
-            load_chunk(sbf, kt, ch, s);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) tmax = fmaxf(tmax, s[i]);
-          }
-          const float mn = fmaxf(m, tmax * p.c);
-          // every lane runs the loads (tcgen05.ld is warp-collective); a row with no
-          // visible key yet adds ex2(-inf) = 0
-          const float mref = mn == -INFINITY ? 0.f : mn;
-          float add = 0.f;
-#pragma unroll 1
-          for (int ch = 0; ch < KT / 32; ++ch) {
-            load_chunk(sbf, kt, ch, s);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) add += ex2(fmaf(s[i], p.c, -mref));
-          }
+          float sv[KT];
+          load_tile(sbf, kt, sv, true);
+          const float mn = fmaxf(m, max128(sv) * p.c);
+          const float mref = mn == -INFINITY ? 0.f : mn;  // a row with no visible key adds 0
+          const float add = exp2_sum128(sv, cc, pk(-mref, -mref));
           if (mn != -INFINITY) {
             l = l * ex2(m - mn) + add;  // ex2(-inf) = 0 for the first finite max
             m = mn;
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar + B_SEMPTY + 8 * sbf);
         }
       }
       // output sweep
@@ -366,20 +420,15 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
       for (int kt = 0; kt < J.nkt; ++kt, ++sc) {
         const int sbf = sc & 1;
         ok = __all_sync(0xffffffffu, ok && ab.wait(bar + B_SFULL + 8 * sbf, (sc >> 1) & 1));
-        float s[32];
+        uint32_t pw[KT / 2];  // P of the row, bf16 pairs
         float alpha = 1.f;
         bool rescale = false;
         if (ok) {
+          float sv[KT];
           tc_fence_after();
+          load_tile(sbf, kt, sv, !wwarp);  // window warps read the scores again below
           if (!fixed) {
-            float tmax = -INFINITY;
-#pragma unroll 1
-            for (int ch = 0; ch < KT / 32; ++ch) {
-              load_chunk(sbf, kt, ch, s);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) tmax = fmaxf(tmax, s[i]);
-            }
-            const float tm = tmax * p.c;
+            const float tm = max128(sv) * p.c;
             if (tm > m + SLACK || (m == -INFINITY && tm != -INFINITY)) {
               alpha = m == -INFINITY ? 0.f : ex2(m - tm);
               rescale = m != -INFINITY;
@@ -387,6 +436,12 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
               m = tm;
             }
           }
+          // P = exp2(s c - m) in place (m = -inf: the row sees no key yet, P = 0)
+          const float nm = m == -INFINITY ? -INFINITY : -m;
+          const float add = exp2_inplace128(sv, cc, pk(nm, nm));
+          if (!fixed) l += add;
+#pragma unroll
+          for (int i = 0; i < KT / 2; ++i) pw[i] = pack_bf16(sv[2 * i], sv[2 * i + 1]);
         }
         // P buffer and O are free once the previous P.V has completed
         if (pc > 0) ok = __all_sync(0xffffffffu, ok && ab.wait(bar + B_PDONE, (pc - 1) & 1));
@@ -404,41 +459,35 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
             }
             tmem_wait_st();
           }
-          const float mref = m;
-#pragma unroll 1
-          for (int ch = 0; ch < KT / 32; ++ch) {
-            load_chunk(sbf, kt, ch, s);
-            float pv[32];
+          // P row, bf16, 128-byte swizzle: keys 64*kb + 8*ci .. + 7 at chunk ci of block kb
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              pv[i] = mref == -INFINITY ? 0.f : ex2(fmaf(s[i], p.c, -mref));
-              if (!fixed) l += pv[i];
-            }
-            // P row, bf16, 128-byte swizzle: keys 64*kb + 8*ci .. + 7 at chunk ci of block kb
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-              const int key = ch * 32 + c8 * 8, kb = key >> 6, ci = (key & 63) >> 3;
-              uint4 w;
-              w.x = pack_bf16(pv[c8 * 8 + 0], pv[c8 * 8 + 1]);
-              w.y = pack_bf16(pv[c8 * 8 + 2], pv[c8 * 8 + 3]);
-              w.z = pack_bf16(pv[c8 * 8 + 4], pv[c8 * 8 + 5]);
-              w.w = pack_bf16(pv[c8 * 8 + 6], pv[c8 * 8 + 7]);
-              *reinterpret_cast<uint4 *>(ptile + kb * Gm::KBLK + r * 128 + ((ci ^ (r & 7)) << 4)) = w;
-            }
-            if (wwarp) {  // window rows: their final probabilities, summed per key
-#pragma unroll
-              for (int i = 0; i < 32; ++i) pv[i] = wrow ? pv[i] * inv_z : 0.f;
-              const float vsum = transpose_reduce32(pv, lane);
-              const int key = kt * KT + ch * 32 + lane;
-              if (key < p.L && vsum != 0.f) atomicAdd(p.votes + (size_t)ukv * p.L + key, vsum);
-            }
+          for (int c8 = 0; c8 < KT / 8; ++c8) {
+            const int kb = c8 >> 3, ci = c8 & 7;
+            const uint4 w = make_uint4(pw[c8 * 4], pw[c8 * 4 + 1], pw[c8 * 4 + 2], pw[c8 * 4 + 3]);
+            *reinterpret_cast<uint4 *>(ptile + kb * Gm::KBLK + r * 128 + ((ci ^ (r & 7)) << 4)) = w;
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P for the MMA
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(bar + B_SEMPTY + 8 * sbf);
-            mbar_arrive(bar + B_PFULL);
+          if (lane == 0) mbar_arrive(bar + B_PFULL);
+          if (wwarp) {
+            // window rows: their final probabilities (the same exp2(s c - m) as P, from
+            // the scores read again), summed per key; then the score buffer is released
+            const float nm = -m;
+#pragma unroll 1
+            for (int ch = 0; ch < KT / 32; ++ch) {
+              float t[32];
+              tmem_ld32(tmem + lane_base + (uint32_t)(sbf * 128 + ch * 32), t);
+              tmem_wait_ld();
+              const int key0 = kt * KT + ch * 32;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                t[i] = (wrow && key0 + i <= row) ? ex2(fmaf(t[i], p.c, nm)) * inv_z : 0.f;
+              const float vsum = transpose_reduce32(t, lane);
+              const int key = key0 + lane;
+              if (key < p.L && vsum != 0.f) atomicAdd(p.votes + (size_t)ukv * p.L + key, vsum);
+            }
+            release(sbf);
           }
         }
         ++pc;

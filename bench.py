@@ -581,7 +581,9 @@ def run_profile_driver(args):
             compact caches (the prompt is freed before the launches);
     aux:    two layers of the H2O (OPT-6.7B) shape, prefill + 4 steps, then two layers
             of the StreamingLLM (Llama-2-13B) shape, fill + 4 steady-state steps;
-    long:   three compressions of two layers of the long-context shape (L = 131072)."""
+    long:   three compressions of two layers of the long-context shape (L = 131072);
+    prefill: three prefill attentions with votes on one layer, batch 1 of the
+            Mistral-7B-shaped prompt (32 query heads, 8 KV heads, L = 16384, D = 128)."""
     import torch
 
     import attention_score_kv_snapkv_gb300 as kvc
@@ -594,6 +596,15 @@ def run_profile_driver(args):
         for _ in range(3):
             kvc.snapkv_compress(x["Q_win"], x["K"], x["V"], keep_window=w.window,
                                 pool_kernel=w.pool_kernel, budget=w.budget, cap=w.budget)
+    elif args.profile == "prefill":
+        import dataclasses
+        w = dataclasses.replace(WL.MISTRAL, batch=1)
+        x = WL.snapkv_prompt(w, 5, dev, layers=1, full_queries=True)
+        out = torch.empty_like(x["Q_full"])
+        votes = torch.empty((1, 1, w.kv_heads, w.prompt_len), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            kvc.snapkv_prefill_attention(x["Q_full"], x["K"], x["V"], window=w.window, out=out,
+                                         votes_out=votes)
     elif args.profile == "decode":
         w = WL.MISTRAL
         x = WL.snapkv_prompt(w, 5, dev)
@@ -891,7 +902,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-aux", action="store_true",
                     help="skip the long-context, H2O and streaming measurements")
-    ap.add_argument("--profile", choices=["decode", "aux", "long"], default=None,
+    ap.add_argument("--profile", choices=["decode", "aux", "long", "prefill"], default=None,
                     help="run a short fixed workload for an ncu capture instead of the bench")
     ap.add_argument("--layers", type=int, default=32, help="profiling only: fewer layers")
     ap.add_argument("--decode-steps", type=int, default=256, help="profiling only")
