@@ -11,11 +11,12 @@
 //   persistent grid (one CTA per SM) in rounds whose CTA order alternates;
 // * warp 0 streams, per job, its Q tile and then K0, V0, K1, V1, ... (keys 0..end of
 //   the tile) through a 4-stage TMA ring (128-byte swizzle); warp 1 issues S = Q.K^T
-//   into one of two TMEM score buffers and O += P.V into a TMEM accumulator (P from
-//   shared memory as bf16, V read MN-major straight from its ring stage); warps 2-5 own
-//   one query row per thread: the row's 128 scores come from TMEM, the online softmax
-//   runs in registers (a row's reference max moves only when the max passes it by more
-//   than 2^8, and then the row of O is rescaled in TMEM), P goes to shared memory;
+//   into one of two TMEM score buffers and O += P.V into a TMEM accumulator (P, bf16,
+//   read as the A operand straight from tensor memory; V read MN-major from its ring
+//   stage); warps 2-5 own one query row per thread: the row's 128 scores come from TMEM
+//   at once, the online softmax runs in registers (a row's reference max moves only when
+//   the max passes it by more than 2^8, and then the row of O is rescaled in TMEM), and
+//   P goes back to tensor memory with tcgen05.st;
 // * a query tile that holds window rows is swept twice: first K only, for each row's
 //   exact max and normaliser, then the output sweep, where those rows' final
 //   probabilities are also summed per key (a transpose-reduce across the warp) and added
@@ -34,20 +35,18 @@ constexpr int NST = 4;         // ring stages (K and V tiles alternate)
 constexpr int NSW = 4;         // softmax warps: one query row per thread
 constexpr int NTH = 32 * (2 + NSW);
 constexpr float SLACK = 8.f;   // log2 headroom before a row's reference max moves
-constexpr int TMEM_COLS = 512; // S0, S1, O
+constexpr int TMEM_COLS = 512; // S0, S1, O, P
 
 template <int D>
 struct PGeo {
   static constexpr int KB = D / 64;
   static constexpr int KBLK = ROWS * 128;       // one 64-column block of a 128-row tile
   static constexpr int TB = KB * KBLK;          // Q, K or V tile bytes
-  static constexpr int PB = (KT / 64) * KBLK;   // P tile bytes (128 rows x 128 keys bf16)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = OFF_Q + TB;
-  static constexpr int OFF_P = OFF_RING + NST * TB;
-  static constexpr int OFF_BAR = OFF_P + PB;
+  static constexpr int OFF_BAR = OFF_RING + NST * TB;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
-  static_assert(TB % 1024 == 0 && PB % 1024 == 0, "swizzled operands stay 1024-aligned");
+  static_assert(TB % 1024 == 0, "swizzled operands stay 1024-aligned");
 };
 
 // barrier offsets (bytes from OFF_BAR)
@@ -116,6 +115,18 @@ __device__ __forceinline__ PJob pjob(const PreP &p, int j) {
   return J;
 }
 
+
+// D (+)= A . B with A (128 x 16 bf16) read from tensor memory: row m on lane m, the 16
+// K values packed two per 32-bit column (8 columns, the lower K index in the low half).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -234,6 +245,7 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tO = tmem + 256;  // O accumulator columns 256 .. 256 + D - 1
+  const uint32_t tP = tmem + 384;  // P of the tile, bf16 pairs: columns 384 .. 447
 
   // jobs of this CTA: rounds of gridDim.x jobs, CTA order reversed on odd rounds
   const int P = gridDim.x, jobs = p.uq * p.nqt;
@@ -311,13 +323,11 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
         if (!ab.wait(bar + B_PFULL, pc & 1)) return false;
         if (!ab.wait(bar + B_FULL + 8 * st, (itv / NST) & 1)) return false;
         tc_fence_after();
-        const uint64_t pd = sdesc_k128(sb + Gm::OFF_P);
         const uint32_t vbase = sb + Gm::OFF_RING + st * Gm::TB;
 #pragma unroll
-        for (int ks = 0; ks < KT / 16; ++ks) {
-          const uint64_t po = (uint64_t)(((ks >> 2) * Gm::KBLK + (ks & 3) * 32) >> 4);
+        for (int ks = 0; ks < KT / 16; ++ks) {  // P from tensor memory, 16 keys (8 columns) a step
           const uint64_t vd = sdesc_mn128(vbase + ks * 16 * 128, Gm::KBLK);
-          umma_bf16(tO, pd + po, vd, id_pv, (!first || ks > 0) ? 1u : 0u);
+          umma_bf16_ts(tO, tP + (uint32_t)(ks * 8), vd, id_pv, (!first || ks > 0) ? 1u : 0u);
         }
         umma_commit(bar + B_EMPTY + 8 * st);
         umma_commit(bar + B_PDONE);
@@ -360,7 +370,6 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    uint8_t *ptile = smem + Gm::OFF_P;
     const unsigned long long cc = pk(p.c, p.c);
     int sc = 0, pc = 0;
     bool ok = true;
@@ -459,14 +468,10 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
             }
             tmem_wait_st();
           }
-          // P row, bf16, 128-byte swizzle: keys 64*kb + 8*ci .. + 7 at chunk ci of block kb
-#pragma unroll
-          for (int c8 = 0; c8 < KT / 8; ++c8) {
-            const int kb = c8 >> 3, ci = c8 & 7;
-            const uint4 w = make_uint4(pw[c8 * 4], pw[c8 * 4 + 1], pw[c8 * 4 + 2], pw[c8 * 4 + 3]);
-            *reinterpret_cast<uint4 *>(ptile + kb * Gm::KBLK + r * 128 + ((ci ^ (r & 7)) << 4)) = w;
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P for the MMA
+          // the P row into tensor memory (lane r, keys 2i and 2i + 1 in column i)
+          tmem_st32(tP + lane_base, reinterpret_cast<const float *>(pw));
+          tmem_st32(tP + lane_base + 32u, reinterpret_cast<const float *>(pw + 32));
+          tmem_wait_st();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar + B_PFULL);
