@@ -85,3 +85,50 @@ def test_prefill_without_votes_and_select_from_votes(kvc):
             idx = torch.as_tensor(a, dtype=torch.long)
             assert torch.equal(sel["k"][0, b, h].cpu(), k[0, b, h, idx])
     assert pooled_gap <= 1
+
+
+def test_prefill_full_size_mistral_sampled(kvc):
+    """The bench's prefill launch (two layers of the Mistral-7B-shaped prompt: batch 2, 32
+    query / 8 KV heads, D 128, L 16384, window 32): sampled output rows against the
+    oracle's attention of that row over keys 0..row, and the votes of sampled KV heads
+    against the oracle's window votes; then selection from those votes against
+    snapkv_compress on the same prompt."""
+    import workloads as W
+    w = W.MISTRAL
+    Ly = 2
+    dev = torch.device("cuda")
+    x = W.snapkv_prompt(w, W.seed_of(2, 7), dev, layers=Ly, full_queries=True)
+    Qf, K, V = x["Q_full"], x["K"], x["V"]
+    L, Wn, G = w.prompt_len, w.window, w.q_heads // w.kv_heads
+    out, votes = kvc.snapkv_prefill_attention(Qf, K, V, window=Wn)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    rng = np.random.default_rng(11)
+    rows = [0, 1, 127, 128, 4095, L - Wn - 1, L - Wn, L - 1] + [int(r) for r in rng.integers(0, L, 8)]
+    for i, row in enumerate(rows):
+        ly, b, hq = i % Ly, (i // 2) % w.batch, int(rng.integers(w.q_heads))
+        h = hq // G
+        ref = OA.attend(f64(Qf[ly, b, hq, row]), f64(K[ly, b, h, :row + 1]), f64(V[ly, b, h, :row + 1]))
+        assert_outputs_close(out[ly, b, hq, row].float().cpu().numpy(), ref,
+                             "output (%d,%d,%d) row %d" % (ly, b, hq, row))
+    for (ly, b, h) in [(0, 0, 0), (Ly - 1, w.batch - 1, w.kv_heads - 1), (1, 0, 5)]:
+        ref = OS.window_votes(f64(Qf[ly, b, h * G:(h + 1) * G, L - Wn:]), f64(K[ly, b, h]))
+        assert_votes_close(votes[ly, b, h].cpu().numpy(), ref, "votes (%d,%d,%d)" % (ly, b, h))
+    kw = dict(keep_window=Wn, pool_kernel=w.pool_kernel, budget=w.budget)
+    sel = kvc.snapkv_select(votes, K, V, **kw)
+    ref = kvc.snapkv_compress(x["Q_win"], K, V, want_votes=True, **kw)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    rel = ((votes - ref["votes"]).abs() / (ref["votes"].abs() + 1e-9)).max().item()
+    assert rel < 1e-5, rel
+    # the kept sets may differ only by swaps at the selection boundary (the two routes'
+    # votes differ by rounding)
+    differ = (sel["pos"] != ref["pos"]).any(dim=-1).nonzero().tolist()
+    assert len(differ) <= 16, len(differ)
+    kp = w.budget - Wn
+    for (ly, b, h) in differ:
+        a, r = sel["pos"][ly, b, h].cpu().numpy(), ref["pos"][ly, b, h].cpu().numpy()
+        pooled = OS.max_pool_1d(ref["votes"][ly, b, h, :L - Wn].double().cpu().numpy(), w.pool_kernel)
+        boundary = np.sort(pooled)[::-1][kp - 1]
+        for j in set(a[:kp].tolist()) ^ set(r[:kp].tolist()):
+            assert abs(pooled[j] - boundary) <= 1e-4 * abs(boundary), (ly, b, h, j)
