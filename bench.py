@@ -376,11 +376,16 @@ def measure_long(kvc, WL, dev, hbm_peak):
             "decode_launch": "eager, one call per step for all layers", "device_status": status}
 
 
-def measure_h2o(kvc, WL, dev, hbm_peak, steps=64):
+def measure_h2o(kvc, WL, dev, hbm_peak, steps=64, n_heavy=None, n_recent=None):
     """H2O on OPT-6.7B shapes (batch 64, 32 layers, 32 MHA heads, prompt 2048, 204 heavy +
-    204 recent): layer-by-layer prefill (scores + cut), then decode steps of all layers."""
+    204 recent, or the given budget): layer-by-layer prefill (scores + cut), then decode
+    steps of all layers."""
+    import dataclasses
+
     import torch
     w = WL.H2O_OPT
+    if n_heavy is not None:
+        w = dataclasses.replace(w, n_heavy=n_heavy, n_recent=n_recent)
     Ly, Bb, H, Dd = w.layers, w.batch, w.kv_heads, w.head_dim
     st = kvc.H2OState(Ly, Bb, H, Dd, w.n_heavy, w.n_recent, dev)
     pre_ms = []
@@ -419,7 +424,8 @@ def measure_h2o(kvc, WL, dev, hbm_peak, steps=64):
     torch.cuda.empty_cache()
     # causal Q.K^T flops of the prefill scores (half the square) per layer
     pre_flops = 2.0 * Bb * w.q_heads * w.prompt_len * w.prompt_len / 2 * Dd
-    return {"workload": w.name, "prefill_ms_per_layer": statistics.median(pre_ms),
+    return {"workload": w.name, "n_heavy": w.n_heavy, "n_recent": w.n_recent,
+            "prefill_ms_per_layer": statistics.median(pre_ms),
             "prefill_causal_qk_TFLOPs": pre_flops / (statistics.median(pre_ms) / 1e3) / 1e12,
             "step_ms": ms, "step_GBps": step_bytes / (ms / 1e3) / 1e9,
             "step_frac_of_hbm_peak": step_bytes / (ms / 1e3) / 1e9 / hbm_peak,
@@ -874,6 +880,10 @@ def run_ours(args):
                        "long_context": measure_long(kvc, WL, dev, hbm_peak),
                        "prefill_with_votes": measure_prefill(kvc, WL, dev, tf_peak),
                        "h2o": measure_h2o(kvc, WL, dev, hbm_peak),
+                       # the other reading of the 20% budget: 20% of the total length
+                       # (prompt 2048 + 2048 generated), 409 heavy + 409 recent
+                       "h2o_budget_total_length": measure_h2o(kvc, WL, dev, hbm_peak, steps=32,
+                                                              n_heavy=409, n_recent=409),
                        "streaming": measure_stream(kvc, WL, dev, hbm_peak),
                        # plain window attention (no sinks) and other sink counts, with the
                        # same 2048-slot cache per head

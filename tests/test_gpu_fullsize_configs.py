@@ -13,6 +13,8 @@ by the fp64 oracle on sampled units:
   the test streams through the first fill and wrap-around, then through that tail.
 """
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -62,8 +64,11 @@ def test_long_context_full_size_sampled(kvc):
     torch.cuda.empty_cache()
 
 
-def test_h2o_full_shape_sampled_lockstep(kvc):
-    w = W.H2O_OPT
+@pytest.mark.parametrize("budget", [(204, 204), (409, 409)], ids=["20pct-of-prompt", "20pct-of-total"])
+def test_h2o_full_shape_sampled_lockstep(kvc, budget):
+    # the budget read as 20% of the prompt (204 + 204) and as 20% of the total length
+    # 4096 (409 + 409)
+    w = dataclasses.replace(W.H2O_OPT, n_heavy=budget[0], n_recent=budget[1])
     Ly, steps = 2, 6
     dev = torch.device("cuda")
     st = kvc.H2OState(Ly, w.batch, w.kv_heads, w.head_dim, w.n_heavy, w.n_recent, dev)
