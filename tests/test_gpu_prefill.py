@@ -18,6 +18,9 @@ CASES = [  # name, Ly, B, Hq, Hkv, D, L, W
     ("one-tile-L128", 1, 2, 2, 1, 128, 128, 8),
     ("window-spans-two-tiles", 1, 1, 2, 1, 128, 400, 160),
     ("gqa4-d128-2layers-L520", 2, 1, 8, 2, 128, 520, 32),
+    ("gqa8-one-kv-head-L260", 1, 1, 8, 1, 128, 260, 16),
+    ("gqa3-d64-odd-group-L333", 1, 1, 6, 2, 64, 333, 24),
+    ("window-is-whole-prompt-L96", 1, 1, 2, 1, 64, 96, 96),
 ]
 
 
