@@ -10,13 +10,15 @@
 // * jobs are (query head, 128-row query tile), heaviest tiles first, spread over a
 //   persistent grid (one CTA per SM) in rounds whose CTA order alternates;
 // * warp 0 streams, per job, its Q tile and then K0, V0, K1, V1, ... (keys 0..end of
-//   the tile) through a 4-stage TMA ring (128-byte swizzle); warp 1 issues S = Q.K^T
-//   into one of two TMEM score buffers and O += P.V into a TMEM accumulator (P, bf16,
-//   read as the A operand straight from tensor memory; V read MN-major from its ring
-//   stage); warps 2-5 own one query row per thread: the row's 128 scores come from TMEM
-//   at once, the online softmax runs in registers (a row's reference max moves only when
-//   the max passes it by more than 2^8, and then the row of O is rescaled in TMEM), and
-//   P goes back to tensor memory with tcgen05.st;
+//   the tile) through two 3-stage TMA rings, one for K and one for V (128-byte swizzle);
+//   warp 1 issues S = Q.K^T into one of two TMEM score buffers, and warp 6 issues
+//   O += P.V into a TMEM accumulator (P, bf16, read as the A operand straight from tensor
+//   memory; V read MN-major from its ring stage): a tcgen05.mma holds its issuing thread
+//   for about its execution time, so the two products get a thread each, and each ring
+//   has one consumer; warps 2-5 own one query row per thread: the row's 128 scores come
+//   from TMEM at once, the online softmax runs in registers (a row's reference max moves
+//   only when the max passes it by more than 2^8, and then the row of O is rescaled in
+//   TMEM), and P goes back to tensor memory with tcgen05.st;
 // * a query tile that holds window rows is swept twice: first K only, for each row's
 //   exact max and normaliser, then the output sweep, where those rows' final
 //   probabilities are also summed per key (a transpose-reduce across the warp) and added
@@ -31,9 +33,11 @@ namespace {
 
 constexpr int ROWS = 128;      // query rows per tile (MMA M)
 constexpr int KT = 128;        // keys per tile (MMA N of S, K of P.V)
-constexpr int NST = 4;         // ring stages (K and V tiles alternate)
+constexpr int NSK = 3;         // K tile ring (consumed by the S issuer only)
+constexpr int NSV = 3;         // V tile ring (consumed by the P.V issuer only)
 constexpr int NSW = 4;         // softmax warps: one query row per thread
-constexpr int NTH = 32 * (2 + NSW);
+constexpr int WPV = 2 + NSW;    // the P.V issuer's warp (after the TMA, S-issuer and softmax warps)
+constexpr int NTH = 32 * (3 + NSW);
 constexpr float SLACK = 8.f;   // log2 headroom before a row's reference max moves
 constexpr int TMEM_COLS = 512; // S0, S1, O, P
 
@@ -43,24 +47,28 @@ struct PGeo {
   static constexpr int KBLK = ROWS * 128;       // one 64-column block of a 128-row tile
   static constexpr int TB = KB * KBLK;          // Q, K or V tile bytes
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_RING = OFF_Q + TB;
-  static constexpr int OFF_BAR = OFF_RING + NST * TB;
+  static constexpr int OFF_RING = OFF_Q + TB;         // K ring
+  static constexpr int OFF_VRING = OFF_RING + NSK * TB;  // V ring
+  static constexpr int OFF_BAR = OFF_VRING + NSV * TB;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static_assert(TB % 1024 == 0, "swizzled operands stay 1024-aligned");
 };
 
 // barrier offsets (bytes from OFF_BAR)
-constexpr int B_FULL = 0;      // [NST] ring stage loaded
-constexpr int B_EMPTY = 32;    // [NST] ring stage read by its MMA (commit)
-constexpr int B_QFULL = 64;    // Q tile loaded
-constexpr int B_QEMPTY = 72;   // the job's MMAs are done with Q (commit)
-constexpr int B_SFULL = 80;    // [2] score buffer written (commit)
-constexpr int B_SEMPTY = 96;   // [2] score buffer read (NSW warps)
-constexpr int B_PFULL = 112;   // P written (NSW warps)
-constexpr int B_PDONE = 120;   // P.V complete: P free, O stable (commit)
-constexpr int B_OFREE = 128;   // the job's O has been read out (NSW warps)
-constexpr int B_ABORT = 136;   // int
-constexpr int B_TMEM = 140;    // uint32
+constexpr int B_FULLK = 0;     // [NSK <= 4] K stage loaded
+constexpr int B_EMPTYK = 32;   // [NSK] K stage read by its S (commit)
+constexpr int B_FULLV = 64;    // [NSV <= 4] V stage loaded
+constexpr int B_EMPTYV = 96;   // [NSV] V stage read by its P.V (commit)
+constexpr int B_QFULL = 128;   // Q tile loaded
+constexpr int B_QEMPTY = 136;  // the job's MMAs are done with Q (commit)
+constexpr int B_SFULL = 144;   // [2] score buffer written (commit)
+constexpr int B_SEMPTY = 160;  // [2] score buffer read (NSW warps)
+constexpr int B_PFULL = 176;   // P written (NSW warps)
+constexpr int B_PDONE = 184;   // P.V complete: P free, O stable (commit)
+constexpr int B_OFREE = 192;   // the job's O has been read out (NSW warps)
+constexpr int B_ABORT = 200;   // int
+constexpr int B_TMEM = 204;    // uint32
+static_assert(NSK <= 4 && NSV <= 4, "ring barrier slots");
 
 struct PreP {
   const __nv_bfloat16 *q;  // [Uq, L, D]
@@ -221,9 +229,13 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(bar + B_FULL + 8 * i, 1);
-      mbar_init(bar + B_EMPTY + 8 * i, 1);
+    for (int i = 0; i < NSK; ++i) {
+      mbar_init(bar + B_FULLK + 8 * i, 1);
+      mbar_init(bar + B_EMPTYK + 8 * i, 1);
+    }
+    for (int i = 0; i < NSV; ++i) {
+      mbar_init(bar + B_FULLV + 8 * i, 1);
+      mbar_init(bar + B_EMPTYV + 8 * i, 1);
     }
     mbar_init(bar + B_QFULL, 1);
     mbar_init(bar + B_QEMPTY, 1);
@@ -256,16 +268,18 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
-      int it = 0;
+      int ik = 0, iv = 0;
       bool ok = true;
-      auto load = [&](const CUtensorMap *map, int row) {
-        const int st = it % NST, use = it / NST;
-        if (!ab.wait(bar + B_EMPTY + 8 * st, (use & 1) ^ 1)) return false;
-        mbar_arrive_expect_tx(bar + B_FULL + 8 * st, Gm::TB);
+      // next K tile into the K ring, or V tile into the V ring (key tile at `row`)
+      auto load = [&](bool isv, int row) {
+        const int n = isv ? NSV : NSK, i = isv ? iv : ik, st = i % n;
+        const uint32_t full = bar + (isv ? B_FULLV : B_FULLK) + 8 * st;
+        if (!ab.wait(bar + (isv ? B_EMPTYV : B_EMPTYK) + 8 * st, ((i / n) & 1) ^ 1)) return false;
+        mbar_arrive_expect_tx(full, Gm::TB);
+        const uint32_t dst = sb + (isv ? Gm::OFF_VRING : Gm::OFF_RING) + st * Gm::TB;
         for (int kb = 0; kb < Gm::KB; ++kb)
-          tma_load_2d(sb + Gm::OFF_RING + st * Gm::TB + kb * Gm::KBLK, map, kb * 64, row,
-                      bar + B_FULL + 8 * st);
-        ++it;
+          tma_load_2d(dst + kb * Gm::KBLK, isv ? &tv : &tk, kb * 64, row, full);
+        if (isv) ++iv; else ++ik;
         return true;
       };
       for (int k = 0; k < njobs && ok; ++k) {
@@ -277,30 +291,36 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
           tma_load_2d(sb + Gm::OFF_Q + kb * Gm::KBLK, &tq, kb * 64, J.uq * p.L + J.qt * ROWS,
                       bar + B_QFULL);
         if (J.twice)
-          for (int kt = 0; kt < J.nkt && ok; ++kt) ok = load(&tk, ukv * p.L + kt * KT);
+          for (int kt = 0; kt < J.nkt && ok; ++kt) ok = load(false, ukv * p.L + kt * KT);
         for (int kt = 0; kt < J.nkt && ok; ++kt) {
-          ok = load(&tk, ukv * p.L + kt * KT);
-          if (ok) ok = load(&tv, ukv * p.L + kt * KT);
+          ok = load(false, ukv * p.L + kt * KT);
+          if (ok) ok = load(true, ukv * p.L + kt * KT);
         }
       }
-      for (int st = 0; st < NST; ++st) {  // drain
-        const int cnt = it / NST + (st < it % NST ? 1 : 0);
-        if (cnt > 0) mbar_wait_bounded(bar + B_FULL + 8 * st, (cnt - 1) & 1, p.timeout);
+      for (int st = 0; st < NSK; ++st) {  // drain
+        const int cnt = ik / NSK + (st < ik % NSK ? 1 : 0);
+        if (cnt > 0) mbar_wait_bounded(bar + B_FULLK + 8 * st, (cnt - 1) & 1, p.timeout);
+      }
+      for (int st = 0; st < NSV; ++st) {
+        const int cnt = iv / NSV + (st < iv % NSV ? 1 : 0);
+        if (cnt > 0) mbar_wait_bounded(bar + B_FULLV + 8 * st, (cnt - 1) & 1, p.timeout);
       }
       if (njobs > 0) mbar_wait_bounded(bar + B_QFULL, (njobs - 1) & 1, p.timeout);
     }
   } else if (warp == 1) {
-    // ------------------------------ MMA issuer ------------------------------
+    // ------------------------------ S issuer ------------------------------
+    // S = Q . K^T per K tile into the two score buffers.  The P.V products have their own
+    // issuer (warp WPV): an MMA's issue holds its thread for about its execution time,
+    // so one thread issuing both would serialise them with its own waits.
     if (lane == 0) {
-      int it = 0, sc = 0, pc = 0;
+      int ik = 0, sc = 0;
       bool ok = true;
       const uint32_t id_s = idesc_bf16(ROWS, KT);
-      const uint32_t id_pv = idesc_bf16(ROWS, D) | (1u << 16);  // B (V) MN-major
       const uint64_t qd = sdesc_k128(sb + Gm::OFF_Q);
-      // S = Q . K^T of the K tile at ring position it, into buffer sc & 1
+      // S of the next K tile, into buffer sc & 1
       auto issue_s = [&]() {
-        const int st = it % NST, sbf = sc & 1;
-        if (!ab.wait(bar + B_FULL + 8 * st, (it / NST) & 1)) return false;
+        const int st = ik % NSK, sbf = sc & 1;
+        if (!ab.wait(bar + B_FULLK + 8 * st, (ik / NSK) & 1)) return false;
         if (!ab.wait(bar + B_SEMPTY + 8 * sbf, ((sc >> 1) & 1) ^ 1)) return false;
         tc_fence_after();
         const uint64_t kd = sdesc_k128(sb + Gm::OFF_RING + st * Gm::TB);
@@ -311,27 +331,10 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
             const uint64_t o = (uint64_t)((kb * Gm::KBLK + kk * 32) >> 4);
             umma_bf16(tmem + (uint32_t)(sbf * 128), qd + o, kd + o, id_s, (kb | kk) != 0);
           }
-        umma_commit(bar + B_EMPTY + 8 * st);
+        umma_commit(bar + B_EMPTYK + 8 * st);
         umma_commit(bar + B_SFULL + 8 * sbf);
-        ++it;
         ++sc;
-        return true;
-      };
-      // O (+)= P . V with the V tile at ring position itv
-      auto issue_pv = [&](int itv, bool first) {
-        const int st = itv % NST;
-        if (!ab.wait(bar + B_PFULL, pc & 1)) return false;
-        if (!ab.wait(bar + B_FULL + 8 * st, (itv / NST) & 1)) return false;
-        tc_fence_after();
-        const uint32_t vbase = sb + Gm::OFF_RING + st * Gm::TB;
-#pragma unroll
-        for (int ks = 0; ks < KT / 16; ++ks) {  // P from tensor memory, 16 keys (8 columns) a step
-          const uint64_t vd = sdesc_mn128(vbase + ks * 16 * 128, Gm::KBLK);
-          umma_bf16_ts(tO, tP + (uint32_t)(ks * 8), vd, id_pv, (!first || ks > 0) ? 1u : 0u);
-        }
-        umma_commit(bar + B_EMPTY + 8 * st);
-        umma_commit(bar + B_PDONE);
-        ++pc;
+        ++ik;
         return true;
       };
       for (int k = 0; k < njobs && ok; ++k) {
@@ -340,25 +343,46 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
         tc_fence_after();
         if (J.twice)
           for (int kt = 0; kt < J.nkt && ok; ++kt) ok = issue_s();
-        // full sweep: S of tile kt, then P.V of tile kt - 1 (the softmax of kt - 1 runs
-        // while S of kt is computed)
-        int itv_prev = -1;
-        for (int kt = 0; kt <= J.nkt && ok; ++kt) {
-          int itv = -1;
-          if (kt < J.nkt) {
-            ok = issue_s();
-            itv = it;  // the V tile follows its K tile in the ring
-            ++it;
-            if (ok && kt == J.nkt - 1) umma_commit(bar + B_QEMPTY);  // Q no longer read
-          }
-          if (ok && kt >= 1) {
-            if (kt == 1 && k > 0 && !ab.wait(bar + B_OFREE, (k - 1) & 1)) { ok = false; break; }
-            ok = issue_pv(itv_prev, kt == 1);
-          }
-          itv_prev = itv;
+        for (int kt = 0; kt < J.nkt && ok; ++kt) {
+          ok = issue_s();
+          if (ok && kt == J.nkt - 1) umma_commit(bar + B_QEMPTY);  // Q no longer read
         }
       }
-      // drain: the last commit (P.V) covers every MMA issued before it
+      // drain: the last commit covers every S this thread issued
+      if (ik > 0) mbar_wait_bounded(bar + B_EMPTYK + 8 * ((ik - 1) % NSK), ((ik - 1) / NSK) & 1, p.timeout);
+    }
+  } else if (warp == WPV) {
+    // ------------------------------ P.V issuer ------------------------------
+    if (lane == 0) {
+      int iv = 0, pc = 0;
+      bool ok = true;
+      const uint32_t id_pv = idesc_bf16(ROWS, D) | (1u << 16);  // B (V) MN-major
+      // O (+)= P . V with the next V tile
+      auto issue_pv = [&](bool first) {
+        const int st = iv % NSV;
+        if (!ab.wait(bar + B_PFULL, pc & 1)) return false;
+        if (!ab.wait(bar + B_FULLV + 8 * st, (iv / NSV) & 1)) return false;
+        tc_fence_after();
+        const uint32_t vbase = sb + Gm::OFF_VRING + st * Gm::TB;
+#pragma unroll
+        for (int ks = 0; ks < KT / 16; ++ks) {  // P from tensor memory, 16 keys (8 columns) a step
+          const uint64_t vd = sdesc_mn128(vbase + ks * 16 * 128, Gm::KBLK);
+          umma_bf16_ts(tO, tP + (uint32_t)(ks * 8), vd, id_pv, (!first || ks > 0) ? 1u : 0u);
+        }
+        umma_commit(bar + B_EMPTYV + 8 * st);
+        umma_commit(bar + B_PDONE);
+        ++pc;
+        ++iv;
+        return true;
+      };
+      for (int k = 0; k < njobs && ok; ++k) {
+        const PJob J = pjob(p, job_of(k));
+        for (int kt = 0; kt < J.nkt && ok; ++kt) {
+          if (kt == 0 && k > 0 && !ab.wait(bar + B_OFREE, (k - 1) & 1)) { ok = false; break; }
+          ok = issue_pv(kt == 0);
+        }
+      }
+      // drain: the last commit (P.V) covers every MMA this thread issued
       if (pc > 0) mbar_wait_bounded(bar + B_PDONE, (pc - 1) & 1, p.timeout);
     }
   } else {
