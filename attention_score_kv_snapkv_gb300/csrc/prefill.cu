@@ -36,7 +36,7 @@ constexpr int KT = 128;        // keys per tile (MMA N of S, K of P.V)
 constexpr int NSK = 3;         // K tile ring (consumed by the S issuer only)
 constexpr int NSV = 3;         // V tile ring (consumed by the P.V issuer only)
 constexpr int NSW = 4;         // softmax warps: one query row per thread
-constexpr int WPV = 2 + NSW;    // the P.V issuer's warp (after the TMA, S-issuer and softmax warps)
+constexpr int WPV = 2 + NSW;   // the P.V issuer's warp (after the TMA, S-issuer and softmax warps)
 constexpr int NTH = 32 * (3 + NSW);
 constexpr float SLACK = 8.f;   // log2 headroom before a row's reference max moves
 constexpr int TMEM_COLS = 512; // S0, S1, O, P
@@ -52,6 +52,7 @@ struct PGeo {
   static constexpr int OFF_BAR = OFF_VRING + NSV * TB;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static_assert(TB % 1024 == 0, "swizzled operands stay 1024-aligned");
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
 // barrier offsets (bytes from OFF_BAR)
