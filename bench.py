@@ -153,6 +153,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, device="cpu"):
+    """Element-wise maximum of `values` over all ranks: the slowest rank sets the whole
+    job's time.  Unchanged without an initialised process group of more than one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def whole_job_rate(units_per_rank, ms_max, world):
+    """Units of all ranks per second, over the slowest rank's time (weak scaling)."""
+    return world * units_per_rank / (ms_max / 1e3)
+
+
 # ------------------------------------------------------------------------------------
 # CPU baseline: the fp64 oracle on a bounded sample of the same workload
 # ------------------------------------------------------------------------------------
@@ -764,10 +781,7 @@ def run_ours(args):
     eb.record(stream)
     torch.cuda.synchronize()
     eager_ms_per_token = ea.elapsed_time(eb) / STEPS
-    if ws > 1:
-        t = torch.tensor([total_ms, comp_avg, dec_avg_step], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, comp_avg, dec_avg_step = (float(v) for v in t.cpu())
+    total_ms, comp_avg, dec_avg_step = max_over_ranks([total_ms, comp_avg, dec_avg_step], dev)
 
     # e2e: the same API with host (pinned) inputs; H2D of Q_win and K and of every decode
     # step's q/k/v, D2H of the final attention output and the cache sizes.  V stays in
@@ -834,7 +848,8 @@ def run_ours(args):
             raise RuntimeError("device status flags %#x after the end-to-end steps" % e2e_status)
         comp_e2e = statistics.median(a.elapsed_time(b) for a, b, c in erec)
         all_e2e = statistics.median(a.elapsed_time(c) for a, b, c in erec)
-        e2e = {"value": ws * B * L / (comp_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        comp_e2e, all_e2e = max_over_ranks([comp_e2e, all_e2e], dev)
+        e2e = {"value": whole_job_rate(B * L, comp_e2e, ws), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": all_e2e,
                "note": "prefix tokens / (H2D of Q_win and K + compression, whose gather reads "
                        "the kept V rows from pinned host memory + D2H of n_valid); "
@@ -845,7 +860,7 @@ def run_ours(args):
     wv_bytes = window_vote_bytes()
     line = {
         "metric": METRIC,
-        "value": ws * B * L / (comp_avg / 1e3),
+        "value": whole_job_rate(B * L, comp_avg, ws),
         "unit": UNIT,
         "n_gpus": ws,
         "steps": args.steps,
