@@ -390,8 +390,9 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
     // ---------------- softmax warps: one query row per thread ----------------
     // A tile's 128 scores of the row are loaded into registers at once (the score
     // buffer is released right away), the row max comes from a three-input max tree,
-    // the exponentials are formed before waiting for the previous P.V (only the bf16
-    // stores of P wait for it), and FFMA / FADD run packed two lanes at a time.
+    // the exponentials are formed and packed to bf16 before waiting for the previous P.V
+    // (only the tcgen05.st of P into tensor memory waits for it), and FFMA / FADD run
+    // packed two lanes at a time.
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
