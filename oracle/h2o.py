@@ -10,7 +10,7 @@ Follows the H2O article (abeam.tech, 2026-06-24):
   the cache updates each cached token's cumulative score; when the cache would exceed
   its budget, everything except the heavy hitters and the recent window is evicted.
 
-Readings where the article is silent (listed in the design doc): the cumulative score
+Readings taken where the article is silent (it gives no formulas): the cumulative score
 starts from the causal column sums of the prompt's own attention; the prompt is cut
 to the top ``n_heavy`` scores before the last ``n_recent`` positions plus those
 ``n_recent`` positions; each step appends the new token, attends over every live

@@ -14,7 +14,7 @@ Follows the SnapKV article (abeam.tech, 2026-07-18), section 処理の流れ
 and section 推論方法 ("inference"): the compression runs once right after the prompt
 is processed, and decoding then reads only the compact cache.
 
-Readings where the article is silent (each is listed with its reason in the design doc):
+Readings taken where the article is silent (it names the steps but gives no formulas):
 softmax over every key a window row may see (prefix plus the causal part of the
 window), scale 1/sqrt(d), plain sum over window rows, selection per KV head with the
 vote summed over the G query heads of the group, max-pool with odd kernel P, stride 1,

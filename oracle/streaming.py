@@ -9,7 +9,7 @@ Follows the StreamingLLM article (abeam.tech, 2026-07-02):
   the oldest recent token is dropped once the window is full, sink tokens are never
   dropped, and attention reads only the sink and recent tokens.
 
-Readings (listed in the design doc): the new token is written before attending, so it
+Readings taken where the article is silent: the new token is written before attending, so it
 attends to itself; before the cache has filled, attention covers all t + 1 tokens;
 the recent region is a ring: token t >= S goes to slot S + (t - S) mod R.
 Position re-indexing inside the cache (a RoPE detail) is not part of this path: keys

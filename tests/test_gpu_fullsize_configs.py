@@ -64,12 +64,14 @@ def test_long_context_full_size_sampled(kvc):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("budget", [(204, 204), (409, 409)], ids=["20pct-of-prompt", "20pct-of-total"])
+@pytest.mark.parametrize("budget", [(204, 204), (409, 409), (204, 4)],
+                         ids=["20pct-of-prompt", "20pct-of-total", "recent4"])
 def test_h2o_full_shape_sampled_lockstep(kvc, budget):
     # the budget read as 20% of the prompt (204 + 204) and as 20% of the total length
-    # 4096 (409 + 409)
+    # 4096 (409 + 409); with a recent window of 4 the decode-appended tokens become
+    # eviction candidates after four steps
     w = dataclasses.replace(W.H2O_OPT, n_heavy=budget[0], n_recent=budget[1])
-    Ly, steps = 2, 6
+    Ly, steps = 2, max(6, budget[1] + 6)
     dev = torch.device("cuda")
     st = kvc.H2OState(Ly, w.batch, w.kv_heads, w.head_dim, w.n_heavy, w.n_recent, dev)
     units = sample_units(Ly, w.batch, w.kv_heads, 4, seed=7)
@@ -97,13 +99,14 @@ def test_h2o_full_shape_sampled_lockstep(kvc, budget):
         out, ev = kvc.h2o_decode_step(q, kn, vn, st, t)
         torch.cuda.synchronize()
         assert kvc.kvc_device_status() == 0
-        gpu_pos = st.pos.cpu().numpy()
+        gpu_pos, gpu_score = st.pos.cpu().numpy(), st.score.cpu().numpy()
         for u in units:
             ly, b, h = u
             swaps += check_step_unit(ref[u], f64(q[ly, b, h:h + 1]), f64(kn[ly, b, h]),
                                      f64(vn[ly, b, h]), t, w.n_recent,
                                      f64(out[ly, b, h:h + 1]), int(ev[ly, b, h]),
-                                     gpu_pos[ly, b, h], "h2o step %d unit %s" % (t, u))
+                                     gpu_pos[ly, b, h], "h2o step %d unit %s" % (t, u),
+                                     gpu_score[ly, b, h])
     assert swaps <= 2
     del st
     torch.cuda.empty_cache()

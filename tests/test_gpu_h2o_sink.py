@@ -41,10 +41,13 @@ def check_prefill_unit(q, K, V, gpu_pos, gpu_score, n_heavy, n_recent):
     return o, swaps
 
 
-def check_step_unit(o, q, k_new, v_new, t, n_recent, gpu_out, gpu_evicted, gpu_pos, what):
+def check_step_unit(o, q, k_new, v_new, t, n_recent, gpu_out, gpu_evicted, gpu_pos, what,
+                    gpu_score=None):
     """One unit's decode step against the oracle state o (advanced in place).  If the GPU
     evicted a different entry, it must be an equally valid choice (score within the band
-    of the minimum); the oracle then follows it.  Returns the number of such swaps."""
+    of the minimum); the oracle then follows it.  With gpu_score (the unit's per-slot
+    cumulative scores after the step) every live entry's score is compared, by position,
+    with the oracle's at the vote tolerance.  Returns the number of such swaps."""
     snap = (o.k.copy(), o.v.copy(), o.score.copy(), o.pos.copy(), o.n_used, o.free_slot)
     ro, rev, cand = OH.step(o, q, k_new, v_new, t, n_recent)
     assert_outputs_close(gpu_out, ro, what)
@@ -59,6 +62,12 @@ def check_step_unit(o, q, k_new, v_new, t, n_recent, gpu_out, gpu_evicted, gpu_p
         OH.step(o, q, k_new, v_new, t, n_recent, evict_override=gsel[0][0])
         swaps = 1
     assert set(gpu_pos[gpu_pos >= 0].tolist()) - {int(gpu_evicted)} == set(o.pos[o.live()].tolist())
+    if gpu_score is not None:
+        live = o.live()
+        by_pos = {int(p): float(s) for p, s in zip(gpu_pos, gpu_score)
+                  if p >= 0 and int(p) != int(gpu_evicted)}
+        assert_votes_close([by_pos[int(p)] for p in o.pos[live]], o.score[live],
+                           what + " cumulative scores")
     return swaps
 
 
@@ -92,20 +101,23 @@ def run_h2o_lockstep(kvc, Ly, B, Hq, Hkv, D, L, n_heavy, n_recent, steps, seed):
         torch.cuda.synchronize()
         assert kvc.kvc_device_status() == 0
         outh, evh = f64(out), ev.cpu().numpy()
-        gpu_pos = st.pos.cpu().numpy()
+        gpu_pos, gpu_score = st.pos.cpu().numpy(), st.score.cpu().numpy()
         qh, knh, vnh = f64(q), f64(kn), f64(vn)
         for (ly, b, h) in units:
             swaps += check_step_unit(ref[(ly, b, h)], qh[ly, b, h * G:(h + 1) * G], knh[ly, b, h],
                                      vnh[ly, b, h], t, n_recent, outh[ly, b, h * G:(h + 1) * G],
                                      evh[ly, b, h], gpu_pos[ly, b, h],
-                                     "h2o step %d unit %s" % (t, (ly, b, h)))
+                                     "h2o step %d unit %s" % (t, (ly, b, h)),
+                                     gpu_score[ly, b, h])
     return swaps
 
 
 def test_h2o_tiny_workload_lockstep(kvc):
+    # 16 steps past the workload's 32, so that the first decode-appended tokens leave the
+    # recent window and become eviction candidates with scores accumulated on the GPU
     w = W.TINY
     swaps = run_h2o_lockstep(kvc, 1, 1, 4, 4, 64, w.prompt_len, w.n_heavy, w.n_recent,
-                             w.decode_steps, seed=W.seed_of(1, 2))
+                             w.decode_steps + 16, seed=W.seed_of(1, 2))
     assert swaps <= 4
 
 
