@@ -49,7 +49,8 @@ class H2OParams(ctypes.Structure):
 
 class H2OStateC(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("score", ctypes.c_void_p),
-                ("pos", ctypes.c_void_p), ("n_used", ctypes.c_void_p), ("free_slot", ctypes.c_void_p)]
+                ("pos", ctypes.c_void_p), ("n_used", ctypes.c_void_p), ("free_slot", ctypes.c_void_p),
+                ("scratch", ctypes.c_void_p), ("scratch_bytes", ctypes.c_size_t)]
 
 
 class SinkParams(ctypes.Structure):
@@ -77,6 +78,7 @@ _SIGS = {
     "compressed_decode_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(DecodeParams), _P, _P, _P, _P,
                                                       _P, _P, _P, _P, _P]),
     "h2o_prefill_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(H2OParams), ctypes.c_int32]),
+    "h2o_step_scratch_bytes": (ctypes.c_size_t, [ctypes.POINTER(H2OParams)]),
     "h2o_prefill": (ctypes.c_int, [ctypes.POINTER(H2OParams), ctypes.c_int32, _P, _P, _P,
                                    ctypes.POINTER(H2OStateC), _P, ctypes.c_size_t, _P]),
     "h2o_decode_step": (ctypes.c_int, [ctypes.POINTER(H2OParams), _P, _P, _P,
@@ -375,7 +377,9 @@ def compressed_decode_attn_noalloc(q, k_cache, v_cache, *, n_valid=None, n_unifo
 
 class H2OState:
     """Device state of an H2O cache: k, v [Ly,B,Hkv,S,D] bf16, score [..,S] fp32,
-    pos [..,S] int32, n_used and free_slot [Ly,B,Hkv] int32, S = n_heavy + n_recent + 1."""
+    pos [..,S] int32, n_used and free_slot [Ly,B,Hkv] int32, S = n_heavy + n_recent + 1,
+    and the zero-filled scratch of the split step (allocated by the first step that asks
+    for it)."""
 
     def __init__(self, n_layers, batch, n_kv_heads, head_dim, n_heavy, n_recent, device):
         S = n_heavy + n_recent + 1
@@ -387,18 +391,22 @@ class H2OState:
         self.pos = torch.full(shp + (S,), -1, dtype=torch.int32, device=device)
         self.n_used = torch.zeros(shp, dtype=torch.int32, device=device)
         self.free_slot = torch.zeros(shp, dtype=torch.int32, device=device)
+        self.scratch = None
 
     def c_struct(self):
+        sc = self.scratch
         return H2OStateC(self.k.data_ptr(), self.v.data_ptr(), self.score.data_ptr(),
-                         self.pos.data_ptr(), self.n_used.data_ptr(), self.free_slot.data_ptr())
+                         self.pos.data_ptr(), self.n_used.data_ptr(), self.free_slot.data_ptr(),
+                         None if sc is None else sc.data_ptr(), 0 if sc is None else sc.numel())
 
     def layer(self, l):
         """A view of layer l alone (the state of a one-layer call, e.g. a layer-by-layer
-        prefill); it shares memory with this state."""
+        prefill); it shares memory (and the scratch) with this state."""
         view = H2OState.__new__(H2OState)
         view.n_heavy, view.n_recent, view.slots = self.n_heavy, self.n_recent, self.slots
-        for name in ("k", "v", "score", "pos", "n_used", "free_slot"):
-            setattr(view, name, getattr(self, name)[l:l + 1])
+        for name in ("k", "v", "score", "pos", "n_used", "free_slot", "scratch"):
+            v = getattr(self, name)
+            setattr(view, name, v if name == "scratch" else v[l:l + 1])
         return view
 
 
@@ -445,6 +453,9 @@ def h2o_decode_step(q, k_new, v_new, state, t, *, out=None, evicted=None, stream
     _need(out, "out", bf, q.shape)
     _need(evicted, "evicted", torch.int32, (Ly, B, Hkv))
     p = H2OParams(Ly, B, q.shape[2], Hkv, D, state.n_heavy, state.n_recent)
+    need = lib().h2o_step_scratch_bytes(ctypes.byref(p))
+    if state.scratch is None or state.scratch.numel() < need:
+        state.scratch = torch.zeros(max(int(need), 256), dtype=torch.uint8, device=q.device)
     st = state.c_struct()
     code = lib().h2o_decode_step(ctypes.byref(p), _ptr(q), _ptr(k_new), _ptr(v_new),
                                  ctypes.byref(st), int(t), _ptr(out), _ptr(evicted),

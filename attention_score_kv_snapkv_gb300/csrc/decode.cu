@@ -37,8 +37,8 @@
 //   A unit covered by one segment is written directly; otherwise each segment's (max,
 //   normaliser, o) goes to the workspace and the last CTA to finish one of the unit's
 //   segments (atomic counter, no waiting) merges them and writes the bf16 output,
-//   resetting the counter.  The counters live in a fixed 256 KB header of the workspace
-//   (one int per unit, at most 65535 units) that is zero between calls, whatever the
+//   resetting the counter.  The counters live in a fixed 512 KB header of the workspace
+//   (one int per unit, at most 131072 units) that is zero between calls, whatever the
 //   call shapes.
 // * every wait is bounded (on expiry the CTA sets the device timeout flag and abandons
 //   its work), and the V reader checks the stage tag as a self-check of the ring.
@@ -131,6 +131,7 @@ struct DecP {
   int n_uniform, cap;
   int units, tiles_per_unit;  // tile slots of ROWS rows per unit (for n <= cap)
   __nv_bfloat16 *out;
+  int ga;                  // query heads per unit in q and out (<= G; heads ga..G-1 pad the MMA)
   float2 *part_ml;         // [U][T][G] per-segment (max, normaliser)
   float *part_o;           // [U][T][G][D] per-segment unnormalised o
   int *cnt;                // [U]
@@ -398,13 +399,14 @@ __global__ void __launch_bounds__(NTH, MINB) decode_kernel(const __grid_constant
     const int vsub = D == 128 ? (lane & 1) * 8 : (lane & 3) * 4;
     int it = 0, sc = 0;
     bool ok = true;
-    // q of unit uu into operand buffer qb: rows 0..G-1, one 16-byte chunk per thread
+    // q of unit uu into operand buffer qb: rows 0..ga-1, one 16-byte chunk per thread
+    // (rows ga..15 stay zero)
     auto write_q = [&](int uu, int qb) {
       uint8_t *qo = smem + Gm::OFF_Q + qb * Gm::QOP;
-      for (int c = t; c < G * D / 8; c += 32 * NCW) {
+      for (int c = t; c < p.ga * D / 8; c += 32 * NCW) {
         const int g = c / (D / 8), ch = c % (D / 8), kb = ch >> 3, ci = ch & 7;
         *reinterpret_cast<uint4 *>(qo + kb * Gm::QBLK + g * 128 + ((ci ^ (g & 7)) << 4)) =
-            *reinterpret_cast<const uint4 *>(p.q + ((size_t)uu * G + g) * D + ch * 8);
+            *reinterpret_cast<const uint4 *>(p.q + ((size_t)uu * p.ga + g) * D + ch * 8);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the tensor cores
       __syncwarp();
@@ -630,7 +632,8 @@ __global__ void __launch_bounds__(NTH, MINB) decode_kernel(const __grid_constant
           for (int w = 0; w < NCW; ++w) O += stg[(size_t)w * G * D + e] * scl[w * G + g];
           const float2 ml = mlv[g];
           if (direct) {
-            p.out[(size_t)u * G * D + e] = __float2bfloat16(ml.y > 0.f ? O / ml.y : 0.f);
+            if (g < p.ga)
+              p.out[((size_t)u * p.ga + g) * D + d] = __float2bfloat16(ml.y > 0.f ? O / ml.y : 0.f);
             if (e < D / 8 && sg.arow >= 0) append_row<D>(p, u, sg.arow, sg.n_old, e);
           } else {
             p.part_o[(((size_t)u * T + sg.iseg) * G + g) * D + d] = O;
@@ -665,7 +668,7 @@ __global__ void __launch_bounds__(NTH, MINB) decode_kernel(const __grid_constant
                 O += o * fs;
               }
             }
-            p.out[(size_t)u * G * D + e] = __float2bfloat16(L > 0.f ? O / L : 0.f);
+            if (g < p.ga) p.out[((size_t)u * p.ga + g) * D + d] = __float2bfloat16(L > 0.f ? O / L : 0.f);
           }
           if (sg.arow >= 0)
             for (int e = te; e < D / 8; e += NE) append_row<D>(p, u, sg.arow, sg.n_old, e);
@@ -723,11 +726,18 @@ cudaError_t launch_t(const Ctx &c, const DecodeArgs &a, DecP p) {
 
 }  // namespace
 
-constexpr size_t CNT_HEADER = 65536 * sizeof(int);  // per-unit counters, zero between calls
+constexpr size_t CNT_HEADER = (size_t)KVC_DECODE_MAX_UNITS * sizeof(int);  // per-unit counters,
+                                                                            // zero between calls
+
+size_t decode_counter_bytes(int units) { return (size_t)units * sizeof(int); }
+
+// Query heads per unit as the kernel instantiates them: G rounded up to 1, 2, 4 or 8.
+int padded_group(int G) { return G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : 8)); }
 
 // Workspace: the counter header, then per unit and segment (at most one segment per
 // tile slot) the partial (max, normaliser) per head and the partial o per head.
 size_t decode_ws_bytes(int units, int G, int D, int cap, int num_sms) {
+  G = padded_group(G);
   const size_t smax = (size_t)(cap > 0 ? (cap + ROWS - 1) / ROWS : 1);
   size_t b = CNT_HEADER;
   b += (size_t)units * smax * G * sizeof(float2);
@@ -757,14 +767,16 @@ cudaError_t launch_decode(const Ctx &c, const DecodeArgs &a) {
   p.units = a.units;
   p.tiles_per_unit = T;
   p.out = reinterpret_cast<__nv_bfloat16 *>(a.out);
+  p.ga = a.G;
+  const int Gp = padded_group(a.G);
   uint8_t *w = reinterpret_cast<uint8_t *>(a.ws);
   p.cnt = reinterpret_cast<int *>(w);
   p.part_ml = reinterpret_cast<float2 *>(w + CNT_HEADER);
-  p.part_o = reinterpret_cast<float *>(w + CNT_HEADER + (size_t)a.units * smax * a.G * sizeof(float2));
+  p.part_o = reinterpret_cast<float *>(w + CNT_HEADER + (size_t)a.units * smax * Gp * sizeof(float2));
   p.status = c.status;
   p.timeout = c.timeout_ns;
 #define KVC_DEC(DD, GG) \
-  if (a.D == DD && a.G == GG) return launch_t<DD, GG>(c, a, p);
+  if (a.D == DD && Gp == GG) return launch_t<DD, GG>(c, a, p);
   KVC_DEC(128, 1) KVC_DEC(128, 2) KVC_DEC(128, 4) KVC_DEC(128, 8)
   KVC_DEC(64, 1) KVC_DEC(64, 2) KVC_DEC(64, 4) KVC_DEC(64, 8)
 #undef KVC_DEC

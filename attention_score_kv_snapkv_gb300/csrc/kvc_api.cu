@@ -233,6 +233,69 @@ namespace {
 void ensure_encode() { std::call_once(g_encode_once, load_encode); }
 }  // namespace
 
+namespace kvc {
+
+// compressed_decode_attn with an option to clear the split-K counters of the workspace
+// first (after every argument check has passed, right before the launch).
+kvc_status decode_call(const kvc_decode_params *p, const void *q, const void *k_new,
+                       const void *v_new, void *k_cache, void *v_cache, int32_t *pos,
+                       int32_t *n_valid, void *out, void *workspace, size_t workspace_bytes,
+                       kvc_stream_t stream, bool clear_counters) {
+  ensure_encode();
+  Ctx c;
+  kvc_status st = get_ctx(stream, &c);
+  if (st != KVC_OK) return st;
+  if (!p) return KVC_ERR_NULL;
+  if (!common_heads_ok(p->n_layers, p->batch, p->n_q_heads, p->n_kv_heads, p->head_dim) ||
+      p->cap < 1)
+    return KVC_ERR_SHAPE;
+  const int G = p->n_q_heads / p->n_kv_heads;
+  if (G > 8) return KVC_ERR_SHAPE;  // query heads per KV head: 1..8
+  const long long units = (long long)p->n_layers * p->batch * p->n_kv_heads;
+  if (units * p->cap > kMaxRows || units > 65535ll * 32768ll) return KVC_ERR_SHAPE;
+  if (p->n_uniform < 0 || p->n_uniform > p->cap) return KVC_ERR_SHAPE;
+  if (!q || !k_cache || !v_cache || !out) return KVC_ERR_NULL;
+  if ((k_new == nullptr) != (v_new == nullptr)) return KVC_ERR_NULL;
+  if (k_new && !n_valid) return KVC_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (k_new && (!aligned16(k_new) || !aligned16(v_new))) || (pos && !aligned4(pos)) ||
+      (n_valid && !aligned4(n_valid)))
+    return KVC_ERR_ALIGN;
+  const size_t need = decode_ws_bytes((int)units, G, p->head_dim, p->cap, c.num_sms);
+  if (!workspace || workspace_bytes < need) return KVC_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return KVC_ERR_ALIGN;
+  if (!g_encode) return KVC_ERR_CUDA;
+  if (units > KVC_DECODE_MAX_UNITS) return KVC_ERR_SHAPE;  // one split-K counter per unit
+  DecodeArgs a;
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.pos = pos;
+  a.n_valid = n_valid;
+  a.out = out;
+  a.ws = workspace;
+  a.units = (int)units;
+  a.G = G;
+  a.D = p->head_dim;
+  a.cap = p->cap;
+  a.n_uniform = p->n_uniform;
+  a.new_pos = p->new_pos;
+  if (clear_counters &&
+      cudaMemsetAsync(workspace, 0, decode_counter_bytes((int)units), c.stream) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  return cuda_status(launch_decode(c, a));
+}
+
+kvc_status device_check(kvc_stream_t stream) {
+  Ctx c;
+  return get_ctx(stream, &c);
+}
+
+
+}  // namespace kvc
+
 extern "C" {
 
 const char *kvc_status_string(kvc_status s) {
@@ -258,6 +321,7 @@ void kvc_set_wait_timeout_ns(uint64_t ns) {
 }
 
 kvc_status kvc_device_status(uint32_t *flags_out, int clear, kvc_stream_t stream) {
+  const TraceRange trace_range("kvc_device_status");
   Ctx c;
   kvc_status st = get_ctx(stream, &c);
   if (st != KVC_OK) return st;
@@ -271,6 +335,7 @@ kvc_status kvc_device_status(uint32_t *flags_out, int clear, kvc_stream_t stream
 }
 
 kvc_status kvc_selftest_wait_timeout(uint32_t timeout_us, kvc_stream_t stream) {
+  const TraceRange trace_range("kvc_selftest_wait_timeout");
   Ctx c;
   kvc_status st = get_ctx(stream, &c);
   if (st != KVC_OK) return st;
@@ -295,6 +360,7 @@ kvc_status snapkv_compress(const kvc_snapkv_params *p, const void *q_win, const 
                            const void *v, void *k_out, void *v_out, int32_t *pos_out,
                            int32_t *n_valid_out, float *votes_out, float *kept_scores_out,
                            void *workspace, size_t workspace_bytes, kvc_stream_t stream) {
+  const TraceRange trace_range("snapkv_compress");
   ensure_encode();
   return run_snapkv(p, q_win, k, v, k_out, v_out, pos_out, n_valid_out, votes_out,
                     kept_scores_out, workspace, workspace_bytes, stream);
@@ -304,6 +370,7 @@ kvc_status snapkv_select(const kvc_snapkv_params *p, const float *votes, const v
                          const void *v, void *k_out, void *v_out, int32_t *pos_out,
                          int32_t *n_valid_out, float *kept_scores_out, void *workspace,
                          size_t workspace_bytes, kvc_stream_t stream) {
+  const TraceRange trace_range("snapkv_select");
   ensure_encode();
   if (!votes) return KVC_ERR_NULL;
   return run_snapkv(p, nullptr, k, v, k_out, v_out, pos_out, n_valid_out, nullptr,
@@ -313,6 +380,7 @@ kvc_status snapkv_select(const kvc_snapkv_params *p, const float *votes, const v
 kvc_status snapkv_prefill_attention(const kvc_snapkv_params *p, const void *q, const void *k,
                                     const void *v, void *o_out, float *votes_out,
                                     kvc_stream_t stream) {
+  const TraceRange trace_range("snapkv_prefill_attention");
   ensure_encode();
   Ctx c;
   kvc_status st = get_ctx(stream, &c);
@@ -355,48 +423,21 @@ kvc_status compressed_decode_attn(const kvc_decode_params *p, const void *q, con
                                   const void *v_new, void *k_cache, void *v_cache, int32_t *pos,
                                   int32_t *n_valid, void *out, void *workspace,
                                   size_t workspace_bytes, kvc_stream_t stream) {
-  ensure_encode();
-  Ctx c;
-  kvc_status st = get_ctx(stream, &c);
-  if (st != KVC_OK) return st;
-  if (!p) return KVC_ERR_NULL;
-  if (!common_heads_ok(p->n_layers, p->batch, p->n_q_heads, p->n_kv_heads, p->head_dim) ||
-      p->cap < 1)
-    return KVC_ERR_SHAPE;
-  const int G = p->n_q_heads / p->n_kv_heads;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return KVC_ERR_SHAPE;
+  const TraceRange trace_range("compressed_decode_attn");
+  return kvc::decode_call(p, q, k_new, v_new, k_cache, v_cache, pos, n_valid, out, workspace,
+                          workspace_bytes, stream, false);
+}
+
+size_t h2o_step_scratch_bytes(const kvc_h2o_params *p) {
+  if (!p || !common_heads_ok(p->n_layers, p->batch, p->n_q_heads, p->n_kv_heads, p->head_dim) ||
+      p->n_heavy < 0 || p->n_recent < 1)
+    return 256;
+  const long long slots = (long long)p->n_heavy + p->n_recent + 1;
+  if (slots > (1 << 20)) return 256;
   const long long units = (long long)p->n_layers * p->batch * p->n_kv_heads;
-  if (units * p->cap > kMaxRows || units > 65535ll * 32768ll) return KVC_ERR_SHAPE;
-  if (p->n_uniform < 0 || p->n_uniform > p->cap) return KVC_ERR_SHAPE;
-  if (!q || !k_cache || !v_cache || !out) return KVC_ERR_NULL;
-  if ((k_new == nullptr) != (v_new == nullptr)) return KVC_ERR_NULL;
-  if (k_new && !n_valid) return KVC_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-      (k_new && (!aligned16(k_new) || !aligned16(v_new))) || (pos && !aligned4(pos)) ||
-      (n_valid && !aligned4(n_valid)))
-    return KVC_ERR_ALIGN;
-  const size_t need = decode_ws_bytes((int)units, G, p->head_dim, p->cap, c.num_sms);
-  if (!workspace || workspace_bytes < need) return KVC_ERR_WORKSPACE;
-  if (!aligned16(workspace)) return KVC_ERR_ALIGN;
-  if (!g_encode) return KVC_ERR_CUDA;
-  if (units > 65535) return KVC_ERR_SHAPE;  // grid.y limit of the decode launch
-  DecodeArgs a;
-  a.q = q;
-  a.k_new = k_new;
-  a.v_new = v_new;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.pos = pos;
-  a.n_valid = n_valid;
-  a.out = out;
-  a.ws = workspace;
-  a.units = (int)units;
-  a.G = G;
-  a.D = p->head_dim;
-  a.cap = p->cap;
-  a.n_uniform = p->n_uniform;
-  a.new_pos = p->new_pos;
-  return cuda_status(launch_decode(c, a));
+  return plan_h2o_split(units, p->n_q_heads / p->n_kv_heads, p->head_dim, (int)slots,
+                        sms_for_sizing())
+      .scratch_bytes;
 }
 
 size_t h2o_prefill_workspace_bytes(const kvc_h2o_params *p, int32_t prompt_len) {
@@ -420,6 +461,7 @@ size_t h2o_prefill_workspace_bytes(const kvc_h2o_params *p, int32_t prompt_len) 
 kvc_status h2o_prefill(const kvc_h2o_params *p, int32_t prompt_len, const void *q, const void *k,
                        const void *v, const kvc_h2o_state *st, void *workspace,
                        size_t workspace_bytes, kvc_stream_t stream) {
+  const TraceRange trace_range("h2o_prefill");
   ensure_encode();
   if (!p || !st) return KVC_ERR_NULL;
   if (p->n_heavy < 0 || p->n_recent < 1) return KVC_ERR_SHAPE;
@@ -453,6 +495,7 @@ kvc_status h2o_prefill(const kvc_h2o_params *p, int32_t prompt_len, const void *
 kvc_status h2o_decode_step(const kvc_h2o_params *p, const void *q, const void *k_new,
                            const void *v_new, const kvc_h2o_state *st, int32_t t, void *out,
                            int32_t *evicted_pos_out, kvc_stream_t stream) {
+  const TraceRange trace_range("h2o_decode_step");
   Ctx c;
   kvc_status r = get_ctx(stream, &c);
   if (r != KVC_OK) return r;
@@ -461,12 +504,18 @@ kvc_status h2o_decode_step(const kvc_h2o_params *p, const void *q, const void *k
       p->n_heavy < 0 || p->n_recent < 1 || t < 0)
     return KVC_ERR_SHAPE;
   const int G = p->n_q_heads / p->n_kv_heads;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return KVC_ERR_SHAPE;
+  if (G > 8) return KVC_ERR_SHAPE;  // query heads per KV head: 1..8
   const long long slots = (long long)p->n_heavy + p->n_recent + 1;
   const long long units = (long long)p->n_layers * p->batch * p->n_kv_heads;
-  const size_t smem = ((size_t)G * p->head_dim + (size_t)G * slots + 8ull * G * p->head_dim) * 4;
-  if (slots > (1 << 20) || smem > 200 * 1024 || units * slots > kMaxRows || units > (1ll << 31) - 1)
+  if (slots > (1 << 20) || units * slots > kMaxRows || units > (1ll << 31) - 1)
     return KVC_ERR_SHAPE;
+  // one CTA per unit, or the unit's cache split over several CTAs
+  const H2OSplitPlan sp = plan_h2o_split(units, G, p->head_dim, (int)slots, c.num_sms);
+  const bool fits1 = h2o_single_fits(G, p->head_dim, slots);
+  const bool have_scratch = st->scratch && st->scratch_bytes >= sp.scratch_bytes;
+  const bool split = sp.feasible && have_scratch && (sp.nsplit > 1 || !fits1);
+  if (!split && !fits1) return sp.feasible ? KVC_ERR_WORKSPACE : KVC_ERR_SHAPE;
+  if (split && (reinterpret_cast<uintptr_t>(st->scratch) & 255u) != 0) return KVC_ERR_ALIGN;
   if (!q || !k_new || !v_new || !out || !st->k || !st->v || !st->score || !st->pos ||
       !st->n_used || !st->free_slot)
     return KVC_ERR_NULL;
@@ -493,12 +542,15 @@ kvc_status h2o_decode_step(const kvc_h2o_params *p, const void *q, const void *k
   a.slots = (int)slots;
   a.n_recent = p->n_recent;
   a.t = t;
+  a.split = split ? 1 : 0;
+  a.scratch = st->scratch;
   return cuda_status(launch_h2o_step(c, a));
 }
 
 kvc_status sink_window_append(const kvc_sink_params *p, const void *k_new, const void *v_new,
                               void *k_cache, void *v_cache, int32_t *pos, int64_t t,
                               kvc_stream_t stream) {
+  const TraceRange trace_range("sink_window_append");
   Ctx c;
   kvc_status r = get_ctx(stream, &c);
   if (r != KVC_OK) return r;

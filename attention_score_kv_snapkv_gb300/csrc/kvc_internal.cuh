@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/kvcompress.h"
@@ -20,6 +21,15 @@ struct Ctx {
   uint32_t *status;              // device status word (KVC_DEV_* bits)
   unsigned long long timeout_ns; // limit of every device-side wait
   int num_sms;
+};
+
+// A named NVTX range around one C-ABI call (shows each entry point on a profiler's
+// timeline; costs nothing measurable when no tool is attached).
+struct TraceRange {
+  explicit TraceRange(const char *name) { nvtxRangePushA(name); }
+  ~TraceRange() { nvtxRangePop(); }
+  TraceRange(const TraceRange &) = delete;
+  TraceRange &operator=(const TraceRange &) = delete;
 };
 
 // ------------------------------------------------------------------------------
@@ -150,6 +160,13 @@ struct Abort {
     return false;
   }
 };
+
+// *ctr += v with release semantics at GPU scope: every write that happens before it in
+// this thread -- including other threads' writes ordered before it by a CTA barrier --
+// is visible to a thread that reads the new count with acquire semantics.
+__device__ __forceinline__ void red_release_gpu(int *ctr, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
+}
 
 // Spin (bounded) until *ctr >= target with acquire semantics at GPU scope.  Gives up early
 // if another CTA has already flagged a timeout in the status word.
@@ -340,11 +357,19 @@ struct WindowVoteArgs {
   void *ws;        // workspace (statistics exchange), WindowVotePlan::ws_bytes bytes
 };
 struct WindowVotePlan {
+  int single = 0;    // 1: the single-pass kernel (window_vote_tmem.cu), 0: two passes
   int row_tiles, jobs, g, ngroups, min_nkt, max_nkt;
+  int qr = 128;      // single pass: query rows per Q tile and per tensor-memory buffer
   size_t ws_bytes;
 };
+// The single-pass plan when every CTA's share of a job fits its tensor memory, else the
+// two-pass plan.
 WindowVotePlan plan_window_vote(int units, int L, int R, int Wq, int num_sms);
 cudaError_t launch_window_vote(const Ctx &c, const WindowVoteArgs &a);
+// window_vote_tmem.cu: false if no group size fits tensor memory.
+bool plan_window_vote_tmem(int units, int L, int R, int Wq, int num_sms, WindowVotePlan *pl);
+cudaError_t launch_window_vote_tmem(const Ctx &c, const WindowVoteArgs &a,
+                                    const WindowVotePlan &pl);
 
 // select.cu: steps 3-4 (pool + top-k + gather).
 struct SelectArgs {
@@ -374,6 +399,8 @@ struct DecodeArgs {
   int units, G, D, cap, n_uniform, new_pos;
 };
 size_t decode_ws_bytes(int units, int G, int D, int cap, int num_sms);
+// bytes at the start of the workspace holding the per-unit split-K counters
+size_t decode_counter_bytes(int units);
 cudaError_t launch_decode(const Ctx &c, const DecodeArgs &a);
 
 // h2o.cu: one H2O decode step.
@@ -387,8 +414,20 @@ struct H2OArgs {
   void *out;            // [U*G, D]
   int32_t *evicted;     // [U] or null
   int units, G, D, slots, n_recent, t;
+  int split;            // 1: the split step (several CTAs per unit) in `scratch`
+  void *scratch;        // plan_h2o_split(...).scratch_bytes, zero between calls
 };
 cudaError_t launch_h2o_step(const Ctx &c, const H2OArgs &a);
+// The split step's geometry: CTAs per unit, rows per CTA, scratch bytes; feasible is
+// false when a CTA's rows would not fit its shared memory.
+struct H2OSplitPlan {
+  int nsplit, chunk;
+  bool feasible;
+  size_t scratch_bytes;
+};
+H2OSplitPlan plan_h2o_split(long long units, int G, int D, int slots, int num_sms);
+// Whether one CTA per unit keeps a unit's logits in shared memory.
+bool h2o_single_fits(int G, int D, long long slots);
 cudaError_t launch_h2o_init_state(const Ctx &c, int32_t *pos, int32_t *n_used,
                                   int32_t *free_slot, const int32_t *n_valid, int units,
                                   int slots);
@@ -403,5 +442,13 @@ cudaError_t run_selftest_wait(const Ctx &c, int *result);
 
 // kvc_api.cu: tensor-map encoding shared by the TMA kernels.
 bool encode_rows_map(CUtensorMap *map, const void *base, uint64_t rows, int D, int box_rows);
+// kvc_api.cu: compressed_decode_attn, optionally clearing the workspace's split-K
+// counters right before the launch (after every argument check has passed).
+kvc_status decode_call(const kvc_decode_params *p, const void *q, const void *k_new,
+                       const void *v_new, void *k_cache, void *v_cache, int32_t *pos,
+                       int32_t *n_valid, void *out, void *workspace, size_t workspace_bytes,
+                       kvc_stream_t stream, bool clear_counters);
+// kvc_api.cu: KVC_OK if the current device is supported (sm_103), else its error.
+kvc_status device_check(kvc_stream_t stream);
 
 }  // namespace kvc

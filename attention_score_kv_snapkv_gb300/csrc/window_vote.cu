@@ -732,6 +732,8 @@ int choose_group(int min_nkt, int max_nkt, long long jobs, int P) {
 
 WindowVotePlan plan_window_vote(int units, int L, int R, int Wq, int num_sms) {
   WindowVotePlan pl;
+  if (plan_window_vote_tmem(units, L, R, Wq, num_sms, &pl)) return pl;
+  pl.single = 0;
   pl.row_tiles = (R + TILE - 1) / TILE;
   pl.jobs = units * pl.row_tiles;
   pl.min_nkt = 1 << 30;
@@ -757,6 +759,8 @@ WindowVotePlan plan_window_vote(int units, int L, int R, int Wq, int num_sms) {
 }
 
 cudaError_t launch_window_vote(const Ctx &c, const WindowVoteArgs &a) {
+  const WindowVotePlan pl = plan_window_vote(a.units, a.L, a.R, a.Wq, c.num_sms);
+  if (pl.single) return launch_window_vote_tmem(c, a, pl);
   int dev = 0;
   cudaGetDevice(&dev);
   const int di = a.D == 128 ? 1 : 0;
@@ -772,7 +776,6 @@ cudaError_t launch_window_vote(const Ctx &c, const WindowVoteArgs &a) {
   if (!encode_rows_map(&tq, a.q, (uint64_t)a.units * a.R, a.D, TILE)) return cudaErrorInvalidValue;
   if (!encode_rows_map(&tk, a.k, (uint64_t)a.units * a.L, a.D, TILE)) return cudaErrorInvalidValue;
 
-  const WindowVotePlan pl = plan_window_vote(a.units, a.L, a.R, a.Wq, c.num_sms);
   int blocks_per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, fn, NTHREADS, smem);
   if (e != cudaSuccess) return e;

@@ -307,9 +307,16 @@ def run_reference(args):
         if i >= warm:
             times.append(t_c)
     per_unit = statistics.median(times)
+    # the rate of the sample, in the workload's unit: each unit stands for B*L/UNITS prefix
+    # tokens of the full workload
     value = B * L / (per_unit * UNITS)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
-            "steps": steps, "warmup": warm, "ms_per_step": 1e3 * per_unit * UNITS,
+            "steps": steps, "warmup": warm,
+            # measured: one step is one sampled unit's compression by the oracle
+            "ms_per_step": 1e3 * per_unit,
+            "step": "1 of the workload's %d (layer,batch,kv-head) units per step (a bounded "
+                    "sample); value = that unit's %d prefix tokens / its time" % (UNITS, B * L // UNITS),
+            "extrapolated_ms_full_workload": 1e3 * per_unit * UNITS,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_dict(),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -612,6 +619,54 @@ def measure_stream(kvc, WL, dev, hbm_peak, steps=256, n_sink=None, ring=None):
             "step_GBps": step_bytes / (ms / 1e3) / 1e9,
             "step_frac_of_hbm_peak": step_bytes / (ms / 1e3) / 1e9 / hbm_peak,
             "steps_timed": steps, "launches_per_step": 2, "device_status": status}
+
+
+def run_host_link(args):
+    """Host-link copy rates behind the end-to-end number (printed as one JSON line): 2 GiB
+    from pinned host memory to the device over 1, 2, 4 and 8 streams, the same as 64 MB
+    copies on one stream, and 2 GiB device to pinned host; best of three, CUDA events."""
+    import torch
+
+    n = 2 * 1024 ** 3
+    h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d = torch.empty(n, dtype=torch.uint8, device="cuda")
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    cur = torch.cuda.current_stream()
+
+    def best(fn):
+        ms = []
+        for _ in range(3):
+            torch.cuda.synchronize()
+            a, b = ev(), ev()
+            a.record(cur)
+            fn()
+            b.record(cur)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        return n / (min(ms) / 1e3) / 1e9
+
+    res = {"bytes": n}
+    for ns in (1, 2, 4, 8):
+        ss = [torch.cuda.Stream() for _ in range(ns)]
+        chunk = n // ns
+
+        def h2d():
+            for i, st in enumerate(ss):
+                st.wait_stream(cur)
+                with torch.cuda.stream(st):
+                    d[i * chunk:(i + 1) * chunk].copy_(h[i * chunk:(i + 1) * chunk], non_blocking=True)
+            for st in ss:
+                cur.wait_stream(st)
+        res["h2d_GBps_streams%d" % ns] = best(h2d)
+
+    def h2d_chunks():
+        c = 64 * 1024 ** 2
+        for i in range(0, n, c):
+            d[i:i + c].copy_(h[i:i + c], non_blocking=True)
+    res["h2d_GBps_64MB_copies_one_stream"] = best(h2d_chunks)
+    res["d2h_GBps"] = best(lambda: h.copy_(d, non_blocking=True))
+    print(json.dumps({"host_link": res}), flush=True)
+    return 0
 
 
 def run_profile_driver(args):
@@ -943,8 +998,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-aux", action="store_true",
                     help="skip the long-context, H2O and streaming measurements")
-    ap.add_argument("--profile", choices=["decode", "aux", "long", "prefill"], default=None,
-                    help="run a short fixed workload for an ncu capture instead of the bench")
+    ap.add_argument("--profile", choices=["decode", "aux", "long", "prefill", "h2d"], default=None,
+                    help="run a short fixed workload for an ncu capture instead of the bench "
+                         "(h2d: measure the host-link copy rates)")
     ap.add_argument("--layers", type=int, default=32, help="profiling only: fewer layers")
     ap.add_argument("--decode-steps", type=int, default=256, help="profiling only")
     args = ap.parse_args()
@@ -955,6 +1011,8 @@ def main():
         for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
             os.environ[v] = "1"  # the oracle runs on one core (set before numpy loads)
         return run_reference(args)
+    if args.profile == "h2d":
+        return run_host_link(args)
     if args.profile:
         return run_profile_driver(args)
     return run_ours(args)

@@ -65,6 +65,12 @@ typedef enum {
 #define KVC_DEV_CACHE_FULL 0x2u  /* an append found its cache full; the token was dropped */
 #define KVC_DEV_BAD_STATE  0x4u  /* an H2O/decode state was inconsistent (e.g. slot out of range) */
 
+/* Limits of the decode-time entry points (compressed_decode_attn, its _noalloc variant
+ * and h2o_decode_step): G = Hq / Hkv query heads per KV head in 1..8; at most
+ * KVC_DECODE_MAX_UNITS units (Ly * B * Hkv) per compressed_decode_attn call (one split-K
+ * counter per unit in the workspace's fixed header). */
+#define KVC_DECODE_MAX_UNITS 131072
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *kvc_status_string(kvc_status s);
 
@@ -201,6 +207,7 @@ size_t compressed_decode_attn_workspace_bytes(const kvc_decode_params *p);
  * workspace: dev, >= compressed_decode_attn_workspace_bytes(p) bytes; it must be
  *   zero-filled before its first use with this function; every call that returns
  *   normally leaves its counters at zero again (after KVC_DEV_TIMEOUT, zero it again).
+ * Limits: G in 1..8 and U <= KVC_DECODE_MAX_UNITS, else KVC_ERR_SHAPE.
  * Errors: as snapkv_compress. */
 kvc_status compressed_decode_attn(const kvc_decode_params *p, const void *q, const void *k_new,
                                   const void *v_new, void *k_cache, void *v_cache, int32_t *pos,
@@ -240,7 +247,15 @@ typedef struct {      /* all dev pointers, owned by the caller */
   int32_t *pos;       /* int32 [U, S_h] token position, -1 = never used */
   int32_t *n_used;    /* int32 [U] live entries after the last step (<= S_h - 1) */
   int32_t *free_slot; /* int32 [U] slot the next token is written to */
+  void *scratch;      /* dev scratch of the split step, h2o_step_scratch_bytes() bytes,
+                         zero-filled before its first use (every step that returns
+                         normally leaves it reusable); may be NULL (see h2o_decode_step) */
+  size_t scratch_bytes;
 } kvc_h2o_state;
+
+/* Bytes of state scratch h2o_decode_step needs to split each unit's cache over several
+ * CTAs (few units, or more slots than one CTA's shared memory holds). */
+size_t h2o_step_scratch_bytes(const kvc_h2o_params *p);
 
 /* Bytes of workspace h2o_prefill needs for a prompt of prompt_len tokens. */
 size_t h2o_prefill_workspace_bytes(const kvc_h2o_params *p, int32_t prompt_len);
@@ -262,7 +277,13 @@ kvc_status h2o_prefill(const kvc_h2o_params *p, int32_t prompt_len, const void *
  * <= t - n_recent (equal scores: the higher position) and make its slot the free slot.
  * q, out: dev bf16 [Ly,B,Hq,D]; k_new, v_new: dev bf16 [Ly,B,Hkv,D];
  * evicted_pos_out: dev int32 [U] (evicted position or -1) or NULL.
- * No workspace.  Errors: as snapkv_compress. */
+ * Split step: with st->scratch of at least h2o_step_scratch_bytes(p) bytes, a call with
+ * few units (less than four CTAs per SM at one CTA per unit) splits each unit's cache
+ * over several CTAs, and so does a cache whose logits do not fit one CTA's shared
+ * memory (4 * (9 * G * D + G * S_h) bytes above 200 KB, i.e. S_h > 50048 at G = 1,
+ * D = 128); the results are those of the one-CTA step up to fp32 rounding.  Without the
+ * scratch such a cache returns KVC_ERR_WORKSPACE.  Limits: G in 1..8, S_h <= 2^20.
+ * Errors: as snapkv_compress. */
 kvc_status h2o_decode_step(const kvc_h2o_params *p, const void *q, const void *k_new,
                            const void *v_new, const kvc_h2o_state *st, int32_t t, void *out,
                            int32_t *evicted_pos_out, kvc_stream_t stream);

@@ -172,10 +172,12 @@ def test_decode_many_tiles_per_cta(kvc, shape, append):
 
 
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_decode_every_head_group_and_dim(kvc, D, G):
-    """Every compiled (D, G) instantiation, with enough units that CTAs stream several
-    tiles and units split between CTAs, ragged row counts and the fused append."""
+    """Every head group G = 1..8 (G = 3, 5, 6, 7 run the next compiled group size with
+    zero query rows padding the MMA) and both head dims, with enough units that CTAs
+    stream several tiles and units split between CTAs, ragged row counts and the fused
+    append."""
     Ly, B, Hkv, cap = 1, 4, 16, 777
     Hq = Hkv * G
     q, kc, vc = rand_cache(Ly, B, Hq, Hkv, D, cap, seed=D * 10 + G)
@@ -196,3 +198,12 @@ def test_decode_every_head_group_and_dim(kvc, D, G):
         vc2[idx + (int(n0[idx]),)] = vn[idx]
     assert torch.equal(nd.cpu(), n0 + 1)
     assert_outputs_close(f64(out), oracle_decode(q, kc2, vc2, (n0 + 1).numpy()))
+
+
+def test_decode_rejects_more_than_eight_heads_per_group(kvc):
+    dev = torch.device("cuda")
+    q = torch.zeros((1, 1, 9, 64), dtype=torch.bfloat16, device=dev)
+    kc = torch.zeros((1, 1, 1, 16, 64), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(kvc.KVCError) as e:
+        kvc.compressed_decode_attn(q, kc, kc, n_uniform=4)
+    assert e.value.code == 2  # KVC_ERR_SHAPE

@@ -126,6 +126,14 @@ def test_h2o_gqa_ragged_lockstep(kvc):
     assert swaps <= 4
 
 
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 6, 7, 8], ids=lambda g: "G%d" % g)
+def test_h2o_every_head_group_lockstep(kvc, G):
+    # two KV heads of G query heads each; the recent window of 6 is passed after six
+    # steps, so decode-appended tokens become eviction candidates
+    swaps = run_h2o_lockstep(kvc, 1, 1, 2 * G, 2, 64, 150, 12, 6, 14, seed=40 + G)
+    assert swaps <= 2
+
+
 def test_h2o_no_eviction_until_full(kvc):
     # prompt shorter than the budget: the cache first fills, then starts evicting
     run_h2o_lockstep(kvc, 1, 1, 2, 2, 64, 10, 8, 4, 10, seed=4)
@@ -190,3 +198,58 @@ def test_sink_count_sweep_gqa(kvc, n_sink):
     assert kvc.kvc_device_status() == 0
     p = pos.cpu().numpy()[0, 1, 1]
     assert sorted(p.tolist()) == sorted(OSt.visible_positions(T - 1, S, R).tolist())
+
+
+@pytest.mark.parametrize("G", [1, 4], ids=["G1-few-units", "G4-logits-exceed-one-cta"])
+def test_h2o_split_step_budget_20pct_of_131072(kvc, G):
+    """The H2O step on a cache of 20% of a 131072-token context (13107 heavy + 13107
+    recent), built directly (a prefill of that prompt is far beyond the oracle), for two
+    KV heads: the step splits each unit's cache over several CTAs (few units; at G = 4
+    the logits would not fit one CTA's shared memory either).  Three steps in lockstep
+    with the oracle: outputs, evicted positions and every live entry's score."""
+    Ly, B, Hkv, D = 1, 1, 2, 128
+    n_heavy = n_recent = 13107
+    S = n_heavy + n_recent + 1
+    t0 = 131072
+    g = torch.Generator().manual_seed(500 + G)
+    dev = torch.device("cuda")
+    st = kvc.H2OState(Ly, B, Hkv, D, n_heavy, n_recent, dev)
+    k = torch.randn((Ly, B, Hkv, S, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((Ly, B, Hkv, S, D), generator=g).to(torch.bfloat16)
+    score = (1.0 + 99.0 * torch.rand((Ly, B, Hkv, S), generator=g)).float()
+    pos = torch.full((Ly, B, Hkv, S), -1, dtype=torch.int32)
+    refs = {}
+    for h in range(Hkv):
+        heavy = torch.randperm(t0 - n_recent, generator=g)[:n_heavy]
+        recent = torch.arange(t0 - n_recent, t0, dtype=torch.int64)
+        allpos = torch.cat([heavy, recent])[torch.randperm(S - 1, generator=g)]
+        pos[0, 0, h, :S - 1] = allpos.int()
+        score[0, 0, h, S - 1] = 0.0
+        o = OH.H2OState(S, D)
+        o.k[:], o.v[:] = f64(k[0, 0, h]), f64(v[0, 0, h])
+        o.score[:], o.pos[:] = f64(score[0, 0, h]), pos[0, 0, h].numpy()
+        o.n_used = o.free_slot = S - 1
+        refs[h] = o
+    st.k.copy_(k)
+    st.v.copy_(v)
+    st.score.copy_(score)
+    st.pos.copy_(pos)
+    st.n_used.fill_(S - 1)
+    st.free_slot.fill_(S - 1)
+    swaps = 0
+    for s in range(3):
+        t = t0 + s
+        q = torch.randn((Ly, B, Hkv * G, D), generator=g).to(torch.bfloat16)
+        kn = torch.randn((Ly, B, Hkv, D), generator=g).to(torch.bfloat16)
+        vn = torch.randn((Ly, B, Hkv, D), generator=g).to(torch.bfloat16)
+        out, ev = kvc.h2o_decode_step(q.to(dev), kn.to(dev), vn.to(dev), st, t)
+        torch.cuda.synchronize()
+        assert kvc.kvc_device_status() == 0
+        outh, evh = f64(out), ev.cpu().numpy()
+        gpos, gscore = st.pos.cpu().numpy(), st.score.cpu().numpy()
+        for h in range(Hkv):
+            swaps += check_step_unit(refs[h], f64(q[0, 0, h * G:(h + 1) * G]), f64(kn[0, 0, h]),
+                                     f64(vn[0, 0, h]), t, n_recent, outh[0, 0, h * G:(h + 1) * G],
+                                     evh[0, 0, h], gpos[0, 0, h], "split step %d head %d" % (t, h),
+                                     gscore[0, 0, h])
+    assert swaps <= 1

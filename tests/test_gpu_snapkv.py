@@ -1,6 +1,8 @@
 """GPU parity of snapkv_compress (window votes, pool + top-k, gather) against the fp64
 oracle on seeded inputs: sizes that span several 128-key tiles, ragged tails, GQA, two
-row tiles, the multi-CTA statistics exchange, and the degenerate budgets."""
+row tiles, the multi-CTA statistics exchange, the degenerate budgets, and shapes served
+by each window-vote kernel (single-pass for jobs of up to 64 rows with enough keys, two
+passes for 128-row jobs)."""
 
 import dataclasses
 
@@ -29,6 +31,14 @@ CASES = [
     # an odd prompt length whose vote rows are mostly misaligned (4-byte loads)
     ("window30-vector-tail", 1, 1, 8, 2, 128, 1000, 30, 7, 200),
     ("odd-length-L1023", 1, 1, 4, 4, 64, 1023, 16, 7, 128),
+    # single-pass window votes with a group exchange: 32 rows (one statistics chunk, two
+    # vote sets), 64 rows and 48 rows (a ragged 16-row chunk)
+    ("mha-rows32-L20000-exchange", 1, 1, 4, 4, 128, 20000, 32, 7, 1024),
+    ("gqa2-rows64-L4096-exchange", 1, 1, 4, 2, 128, 4096, 32, 7, 256),
+    ("gqa3-rows48-L3000-exchange", 1, 1, 6, 2, 64, 3000, 16, 5, 200),
+    # 128 window rows against 80000 keys: the two-pass window-vote kernel (as for every
+    # job of 128 rows)
+    ("two-pass-kernel-L80000", 1, 1, 4, 1, 128, 80000, 32, 7, 1024),
 ]
 
 

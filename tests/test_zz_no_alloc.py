@@ -5,14 +5,18 @@ device).  Its split-K scratch is the library's fixed 8 MiB device array.
 
 Checks, through the C ABI: two calls in a row agree with compressed_decode_attn (which
 takes a caller workspace) within the decode tolerance, with and without the fused
-append, and a call that would need more scratch than the array holds is rejected
-with KVC_ERR_WORKSPACE.  This file is collected last on purpose."""
+append, and with the fp64 oracle's attention directly; a call that would need more
+scratch than the array holds is rejected with KVC_ERR_WORKSPACE, and a call rejected by
+an argument check returns its error without disturbing the next call.  The file name sorts last so that a run stopping at its
+first failure has run every other test before this one; the tests themselves depend on
+no order."""
 
 import ctypes
 
 import pytest
 import torch
 
+from oracle import attention as OA
 from parity import assert_outputs_close, f64
 
 pytestmark = pytest.mark.gpu
@@ -42,12 +46,25 @@ def _noalloc_call(kvc, q, kc, vc, n, out, k_new=None, v_new=None, pos=None, new_
                          ids=["gqa4-d128-cap1280", "mha-d64-cap300"])
 def test_noalloc_matches_workspace_entry_point_twice(kvc, shape):
     q, kc, vc, n = _inputs(*shape, seed=shape[-1])
+    Ly, B, Hq, Hkv = shape[:4]
+    G = Hq // Hkv
+    qh, kh, vh, nh = f64(q), f64(kc), f64(vc), n.cpu().numpy()
     for call in range(2):
         ref = kvc.compressed_decode_attn(q, kc, vc, n_valid=n)
         out = torch.empty_like(q)
         assert _noalloc_call(kvc, q, kc, vc, n, out) == 0
         torch.cuda.synchronize()
         assert_outputs_close(f64(out), f64(ref), "no-alloc call %d" % call)
+        # and directly against the oracle's attention over each unit's first n rows
+        outh = f64(out)
+        for ly in range(Ly):
+            for b in range(B):
+                for h in range(Hkv):
+                    m = int(nh[ly, b, h])
+                    want = OA.attend_group(qh[ly, b, h * G:(h + 1) * G], kh[ly, b, h, :m],
+                                           vh[ly, b, h, :m])
+                    assert_outputs_close(outh[ly, b, h * G:(h + 1) * G], want,
+                                         "no-alloc call %d unit %s" % (call, (ly, b, h)))
     assert kvc.kvc_device_status() == 0
 
 
@@ -81,3 +98,19 @@ def test_noalloc_rejects_calls_beyond_the_fixed_scratch(kvc):
     code = kvc.lib().compressed_decode_attn_noalloc(ctypes.byref(p), None, None, None, None, None,
                                                     None, None, None, None)
     assert code == 7  # KVC_ERR_WORKSPACE, nothing launched
+
+
+def test_rejected_call_leaves_the_scratch_alone(kvc):
+    # a call rejected by an argument check (a misaligned output) between two good calls
+    # returns KVC_ERR_ALIGN, and the next call still matches the workspace entry point
+    q, kc, vc, n = _inputs(1, 2, 16, 4, 128, 700, seed=21)
+    out = torch.empty_like(q)
+    assert _noalloc_call(kvc, q, kc, vc, n, out) == 0
+    bad = torch.empty(out.numel() + 8, dtype=out.dtype, device=out.device)[1:1 + out.numel()]
+    p_code = _noalloc_call(kvc, q, kc, vc, n, bad.view(out.shape))
+    assert p_code == 3  # KVC_ERR_ALIGN
+    ref = kvc.compressed_decode_attn(q, kc, vc, n_valid=n)
+    assert _noalloc_call(kvc, q, kc, vc, n, out) == 0
+    torch.cuda.synchronize()
+    assert_outputs_close(f64(out), f64(ref), "no-alloc call after a rejected one")
+    assert kvc.kvc_device_status() == 0
