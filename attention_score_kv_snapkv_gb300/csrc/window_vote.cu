@@ -562,11 +562,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (lane == 0) mbar_arrive(ctl + C_XFULL + 8 * xb);
           }
         } else {
-          // publish this CTA's partial statistics; the consumers combine all g of them
+          // publish this CTA's partial statistics (the barrier orders every thread's
+          // store before the one releasing arrival); the consumers combine all g of them
           p.part[((size_t)j * p.g + xg) * TILE + lrow] = make_float2(m, z);
-          __threadfence();
           named_bar(4, 128);
-          if (lrow == 0) atomicAdd(&p.arrive[j], 1);
+          if (lrow == 0) red_release_gpu(&p.arrive[j], 1);
         }
       }
     }
