@@ -324,8 +324,9 @@ __global__ void __launch_bounds__(NT) h2o_split_kernel(const H2OSplitP sp) {
     qs[e] = __bfloat162float(p.q[(size_t)u * G * D + e]) * p.c;
   __syncthreads();
 
-  // 1. logits of rows e0..e1-1 (layout as in h2o_step_kernel)
-  constexpr int LPR = D / 8, RPL = 32 / LPR, NB = 4;
+  // 1. logits of rows e0..e1-1 (layout as in h2o_step_kernel; eight loads in flight per
+  // lane when the query registers leave room)
+  constexpr int LPR = D / 8, RPL = 32 / LPR, NB = G <= 2 ? 8 : 4;
   const int sub = lane / LPR, ch = lane % LPR;
   float qreg[G][8];
 #pragma unroll
@@ -591,9 +592,9 @@ cudaError_t launch_t(const Ctx &c, const H2OArgs &a, const H2OP &p) {
 H2OSplitPlan plan_h2o_split(long long units, int G, int D, int slots, int num_sms) {
   H2OSplitPlan pl;
   const int nsm = num_sms > 0 ? num_sms : 1;
-  // enough CTAs for four per SM, at least 64 rows each, and few enough rows per CTA
+  // enough CTAs for eight per SM, at least 64 rows each, and few enough rows per CTA
   // that its logits fit shared memory next to the query and the reduction buffers
-  long long want = (4LL * nsm + units - 1) / units;
+  long long want = (8LL * nsm + units - 1) / units;
   const long long by_rows = (slots + 63) / 64;
   if (want > by_rows) want = by_rows;
   const long long cap_rows = (200 * 1024 / 4 - 9LL * G * D) / G;  // logits per CTA that fit

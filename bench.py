@@ -81,6 +81,25 @@ def decode_traffic(rows_per_launch_avg):
         return None
 
 
+def compress_traffic():
+    """dram read + write bytes of one compression of all layers (window vote, pool/top-k
+    and gather launches) from the committed ncu capture; None if the kernel sources
+    changed since the capture or the layer count differs."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "compress_traffic.json")) as f:
+            j = json.load(f)
+        h = hashlib.sha256()
+        for name in ("window_vote.cu", "window_vote_tmem.cu", "select.cu", "kvc_internal.cuh"):
+            with open(os.path.join(ROOT, "attention_score_kv_snapkv_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != j["sources_sha256"] or j["units"] != UNITS:
+            return None
+        return sum(k["dram_read_bytes"] + k["dram_write_bytes"] for k in j["kernels"])
+    except Exception:
+        return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -472,6 +491,68 @@ def measure_h2o(kvc, WL, dev, hbm_peak, steps=64, n_heavy=None, n_recent=None):
             "steps_timed": steps, "device_status": status}
 
 
+def h2o_built_state(kvc, dev, layers, heads, head_dim, n_heavy, n_recent, t0, seed):
+    """An H2O cache of every slot filled (random K/V, scores, distinct positions with the
+    last n_recent positions recent), built directly: a prefill of a prompt that long would
+    only be timed here, not needed."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    S = n_heavy + n_recent + 1
+    st = kvc.H2OState(layers, 1, heads, head_dim, n_heavy, n_recent, dev)
+    st.k.copy_(torch.randn(st.k.shape, generator=g, device=dev).to(torch.bfloat16))
+    st.v.copy_(torch.randn(st.v.shape, generator=g, device=dev).to(torch.bfloat16))
+    st.score.copy_(1.0 + 99.0 * torch.rand(st.score.shape, generator=g, device=dev))
+    heavy = torch.randperm(t0 - n_recent, generator=g, device=dev)[:n_heavy]
+    recent = torch.arange(t0 - n_recent, t0, device=dev)
+    pos = torch.cat([heavy, recent, torch.tensor([-1], device=dev)]).to(torch.int32)
+    st.pos.copy_(pos.expand(st.pos.shape))
+    st.n_used.fill_(S - 1)
+    st.free_slot.fill_(S - 1)
+    return st
+
+
+def measure_h2o_long_budget(kvc, WL, dev, hbm_peak, steps=32):
+    """H2O steps with a budget of 20% of a 131072-token context (13107 heavy + 13107
+    recent) on the long-context shapes (batch 1, 8 layers, 32 heads, D 128): 256 units of
+    26215 slots, too few units for one CTA each to fill the GPU, so the step splits every
+    unit's cache over several CTAs."""
+    import torch
+    w = WL.LONG
+    nh = nr = w.prompt_len // 10
+    t0 = w.prompt_len
+    st = h2o_built_state(kvc, dev, w.layers, w.kv_heads, w.head_dim, nh, nr, t0, 31)
+    g = torch.Generator(device=dev)
+    g.manual_seed(32)
+    q = torch.randn((w.layers, 1, w.q_heads, w.head_dim), generator=g, device=dev).to(torch.bfloat16)
+    kn = torch.randn((w.layers, 1, w.kv_heads, w.head_dim), generator=g, device=dev).to(torch.bfloat16)
+    vn = torch.randn_like(kn)
+    out = torch.empty_like(q)
+    ev = torch.empty((w.layers, 1, w.kv_heads), dtype=torch.int32, device=dev)
+    for s in range(4):
+        kvc.h2o_decode_step(q, kn, vn, st, t0 + s, out=out, evicted=ev)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for s in range(steps):
+        kvc.h2o_decode_step(q, kn, vn, st, t0 + 4 + s, out=out, evicted=ev)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    n = nh + nr + 1
+    units = w.layers * w.kv_heads
+    step_bytes = units * (n * (4 * w.head_dim + 12) + 8 * w.head_dim)
+    status = kvc.kvc_device_status()
+    del st
+    torch.cuda.empty_cache()
+    return {"workload": "h2o budget 20%% of %d tokens (%d heavy + %d recent), %d layers x %d heads, "
+                        "batch 1, D %d" % (t0, nh, nr, w.layers, w.kv_heads, w.head_dim),
+            "units": units, "slots_per_unit": n, "step_ms": ms,
+            "step_GBps": step_bytes / (ms / 1e3) / 1e9,
+            "step_frac_of_hbm_peak": step_bytes / (ms / 1e3) / 1e9 / hbm_peak,
+            "steps_timed": steps, "device_status": status}
+
+
 def measure_budget(kvc, Q, K, V, budget, hbm_peak, reps=5):
     """Compression of the headline prompt at another budget (the cache holds exactly the
     budget): CUDA-event time per call after two warm-up calls."""
@@ -671,6 +752,8 @@ def run_host_link(args):
 
 def run_profile_driver(args):
     """Short fixed workloads for ncu captures (no timing printed):
+    h2o-split: four H2O steps of one layer with a cache of 20% of a 131072-token context
+            (32 units of 26215 slots: the split step);
     decode: four launches of the 32-layer Mistral-shaped decode at n = 1100 on the
             compact caches (the prompt is freed before the launches);
     aux:    two layers of the H2O (OPT-6.7B) shape, prefill + 4 steps, then two layers
@@ -699,6 +782,15 @@ def run_profile_driver(args):
         for _ in range(3):
             kvc.snapkv_prefill_attention(x["Q_full"], x["K"], x["V"], window=w.window, out=out,
                                          votes_out=votes)
+    elif args.profile == "h2o-split":
+        # one layer of the H2O cache at 20% of a 131072-token context: 32 units of 26215
+        # slots, each split over several CTAs; four steps
+        w = WL.LONG
+        st = h2o_built_state(kvc, dev, 1, w.kv_heads, w.head_dim, w.prompt_len // 10,
+                             w.prompt_len // 10, w.prompt_len, 31)
+        q, kn, vn = WL.decode_token(w, 0, 5, dev, layers=1)
+        for s in range(4):
+            kvc.h2o_decode_step(q, kn, vn, st, w.prompt_len + s)
     elif args.profile == "decode":
         w = WL.MISTRAL
         x = WL.snapkv_prompt(w, 5, dev)
@@ -946,7 +1038,10 @@ def run_ours(args):
                               "bound": "hbm", "achieved": compress_bytes() / (comp_avg / 1e3) / 1e9,
                               "peak": hbm_peak, "unit": "GB/s",
                               "frac": compress_bytes() / (comp_avg / 1e3) / 1e9 / hbm_peak,
-                              "algorithmic_bytes": compress_bytes()},
+                              "algorithmic_bytes": compress_bytes(),
+                              "traffic": compress_traffic(),
+                              "traffic_source": "profiles/compress_traffic.json (ncu dram bytes of "
+                                                "the three launches of one %d-layer compression)" % LY},
         "gpu_launches": args.steps * (3 + STEPS),
         "device_status": status,
         "clocks": clk,
@@ -970,6 +1065,7 @@ def run_ours(args):
                        # (prompt 2048 + 2048 generated), 409 heavy + 409 recent
                        "h2o_budget_total_length": measure_h2o(kvc, WL, dev, hbm_peak, steps=32,
                                                               n_heavy=409, n_recent=409),
+                       "h2o_budget_20pct_of_131072": measure_h2o_long_budget(kvc, WL, dev, hbm_peak),
                        "streaming": measure_stream(kvc, WL, dev, hbm_peak),
                        # plain window attention (no sinks) and other sink counts, with the
                        # same 2048-slot cache per head
@@ -998,7 +1094,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-aux", action="store_true",
                     help="skip the long-context, H2O and streaming measurements")
-    ap.add_argument("--profile", choices=["decode", "aux", "long", "prefill", "h2d"], default=None,
+    ap.add_argument("--profile", choices=["decode", "aux", "long", "prefill", "h2d", "h2o-split"],
+                    default=None,
                     help="run a short fixed workload for an ncu capture instead of the bench "
                          "(h2d: measure the host-link copy rates)")
     ap.add_argument("--layers", type=int, default=32, help="profiling only: fewer layers")

@@ -278,7 +278,7 @@ kvc_status h2o_prefill(const kvc_h2o_params *p, int32_t prompt_len, const void *
  * q, out: dev bf16 [Ly,B,Hq,D]; k_new, v_new: dev bf16 [Ly,B,Hkv,D];
  * evicted_pos_out: dev int32 [U] (evicted position or -1) or NULL.
  * Split step: with st->scratch of at least h2o_step_scratch_bytes(p) bytes, a call with
- * few units (less than four CTAs per SM at one CTA per unit) splits each unit's cache
+ * few units (less than eight CTAs per SM at one CTA per unit) splits each unit's cache
  * over several CTAs, and so does a cache whose logits do not fit one CTA's shared
  * memory (4 * (9 * G * D + G * S_h) bytes above 200 KB, i.e. S_h > 50048 at G = 1,
  * D = 128); the results are those of the one-CTA step up to fp32 rounding.  Without the
