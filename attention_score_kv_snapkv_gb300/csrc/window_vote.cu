@@ -278,10 +278,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // causal prefill of H2O), a group's jobs then mix small and large tiles instead of
   // repeating the same few row-tile sizes.  CTAs past the last whole group (when g does
   // not divide the grid) have no jobs.
+  // With several row tiles per unit and at least 8 units per group, a group takes whole
+  // units instead (units gamma, gamma + ngroups, ..., each unit's row tiles in order): a
+  // unit's keys are then re-read by one group while they are still in L2, and every
+  // group gets the same mix of row-tile sizes.
+  const int units = p.jobs / p.row_tiles;
+  const bool unit_major = p.row_tiles > 1 && units >= 8 * p.ngroups;
   const int full_rounds = p.jobs / p.ngroups, rem = p.jobs - full_rounds * p.ngroups;
   const int njobs = gamma >= p.ngroups ? 0
+                    : unit_major ? ((units - gamma + p.ngroups - 1) / p.ngroups) * p.row_tiles
                     : full_rounds + ((full_rounds & 1) ? (p.ngroups - 1 - gamma < rem) : (gamma < rem));
   auto job_of = [&](int kk) {
+    if (unit_major) return (gamma + (kk / p.row_tiles) * p.ngroups) * p.row_tiles + kk % p.row_tiles;
     return kk * p.ngroups + ((kk & 1) ? p.ngroups - 1 - gamma : gamma);
   };
 
