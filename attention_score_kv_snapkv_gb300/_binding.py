@@ -79,6 +79,7 @@ _SIGS = {
                                                       _P, _P, _P, _P, _P]),
     "h2o_prefill_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(H2OParams), ctypes.c_int32]),
     "h2o_step_scratch_bytes": (ctypes.c_size_t, [ctypes.POINTER(H2OParams)]),
+    "h2o_step_ctas_per_unit": (ctypes.c_int32, [ctypes.POINTER(H2OParams)]),
     "h2o_prefill": (ctypes.c_int, [ctypes.POINTER(H2OParams), ctypes.c_int32, _P, _P, _P,
                                    ctypes.POINTER(H2OStateC), _P, ctypes.c_size_t, _P]),
     "h2o_decode_step": (ctypes.c_int, [ctypes.POINTER(H2OParams), _P, _P, _P,
@@ -435,6 +436,13 @@ def h2o_prefill(q, k, v, *, n_heavy, n_recent, state=None, workspace_buf=None, s
                              _ptr(ws), ws.numel(), _stream(stream))
     _check(code, "h2o_prefill")
     return state
+
+
+def h2o_step_ctas_per_unit(n_layers, batch, n_q_heads, n_kv_heads, head_dim, n_heavy, n_recent):
+    """CTAs per unit of the H2O step on the current device (1: one CTA per unit; more: the
+    split step), 0 if the sizes are out of range."""
+    p = H2OParams(n_layers, batch, n_q_heads, n_kv_heads, head_dim, n_heavy, n_recent)
+    return lib().h2o_step_ctas_per_unit(ctypes.byref(p))
 
 
 def h2o_decode_step(q, k_new, v_new, state, t, *, out=None, evicted=None, stream=None):

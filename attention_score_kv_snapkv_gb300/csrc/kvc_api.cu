@@ -440,6 +440,20 @@ size_t h2o_step_scratch_bytes(const kvc_h2o_params *p) {
       .scratch_bytes;
 }
 
+int32_t h2o_step_ctas_per_unit(const kvc_h2o_params *p) {
+  if (!p || !common_heads_ok(p->n_layers, p->batch, p->n_q_heads, p->n_kv_heads, p->head_dim) ||
+      p->n_heavy < 0 || p->n_recent < 1 || p->n_q_heads / p->n_kv_heads > 8)
+    return 0;
+  const long long slots = (long long)p->n_heavy + p->n_recent + 1;
+  if (slots > (1 << 20)) return 0;
+  const long long units = (long long)p->n_layers * p->batch * p->n_kv_heads;
+  const int G = p->n_q_heads / p->n_kv_heads;
+  const H2OSplitPlan sp = plan_h2o_split(units, G, p->head_dim, (int)slots, sms_for_sizing());
+  const bool fits1 = h2o_single_fits(G, p->head_dim, slots);
+  if (sp.feasible && (sp.nsplit > 1 || !fits1)) return sp.nsplit;
+  return fits1 ? 1 : 0;
+}
+
 size_t h2o_prefill_workspace_bytes(const kvc_h2o_params *p, int32_t prompt_len) {
   if (!p) return 256;
   kvc_snapkv_params s;

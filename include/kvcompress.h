@@ -257,6 +257,11 @@ typedef struct {      /* all dev pointers, owned by the caller */
  * CTAs (few units, or more slots than one CTA's shared memory holds). */
 size_t h2o_step_scratch_bytes(const kvc_h2o_params *p);
 
+/* CTAs that h2o_decode_step gives each unit on the current device when the state has its
+ * scratch: 1 for the one-CTA step, more for the split step; 0 if p is out of range.
+ * Host-only (no launch); for callers that size grids or check which step runs. */
+int32_t h2o_step_ctas_per_unit(const kvc_h2o_params *p);
+
 /* Bytes of workspace h2o_prefill needs for a prompt of prompt_len tokens. */
 size_t h2o_prefill_workspace_bytes(const kvc_h2o_params *p, int32_t prompt_len);
 

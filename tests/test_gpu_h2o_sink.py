@@ -114,8 +114,11 @@ def run_h2o_lockstep(kvc, Ly, B, Hq, Hkv, D, L, n_heavy, n_recent, steps, seed):
 
 def test_h2o_tiny_workload_lockstep(kvc):
     # 16 steps past the workload's 32, so that the first decode-appended tokens leave the
-    # recent window and become eviction candidates with scores accumulated on the GPU
+    # recent window and become eviction candidates with scores accumulated on the GPU.
+    # The workload's 4 units are few: the step splits each over several CTAs (more CTAs
+    # than units)
     w = W.TINY
+    assert kvc.h2o_step_ctas_per_unit(1, 1, 4, 4, 64, w.n_heavy, w.n_recent) > 1
     swaps = run_h2o_lockstep(kvc, 1, 1, 4, 4, 64, w.prompt_len, w.n_heavy, w.n_recent,
                              w.decode_steps + 16, seed=W.seed_of(1, 2))
     assert swaps <= 4
@@ -198,6 +201,16 @@ def test_sink_count_sweep_gqa(kvc, n_sink):
     assert kvc.kvc_device_status() == 0
     p = pos.cpu().numpy()[0, 1, 1]
     assert sorted(p.tolist()) == sorted(OSt.visible_positions(T - 1, S, R).tolist())
+
+
+def test_h2o_step_plans(kvc):
+    # one CTA per unit for the OPT-shaped workload (65536 units), several for few units,
+    # the split step for logits beyond one CTA's shared memory, 0 out of range
+    assert kvc.h2o_step_ctas_per_unit(32, 64, 32, 32, 128, 204, 204) == 1
+    assert kvc.h2o_step_ctas_per_unit(8, 1, 32, 32, 128, 13107, 13107) > 1
+    assert kvc.h2o_step_ctas_per_unit(256, 64, 32, 8, 128, 13107, 13107) > 1  # G 4: too wide
+    assert kvc.h2o_step_ctas_per_unit(1, 1, 36, 4, 128, 8, 8) == 0          # G 9
+    assert kvc.h2o_step_ctas_per_unit(1, 1, 4, 4, 128, 8, 0) == 0           # no recent window
 
 
 @pytest.mark.parametrize("G", [1, 4], ids=["G1-few-units", "G4-logits-exceed-one-cta"])
