@@ -66,3 +66,25 @@ def causal_prefill(Q, K, V):
     for i in range(L):
         O[i] = attend(Q[i], K[: i + 1], V[: i + 1])
     return O
+
+
+def log_sum_exp(logits):
+    """ln sum_j exp(x_j) of a 1-D fp64 vector (-inf entries add nothing): the logarithm of
+    the softmax normaliser, so that softmax(x)_j = exp(x_j - log_sum_exp(x)).  Written out
+    with the maximum finite logit taken out first."""
+    x = np.asarray(logits, dtype=np.float64)
+    finite = np.isfinite(x)
+    if not finite.any():
+        raise ValueError("log-sum-exp over an empty key set")
+    m = x[finite].max()
+    return m + np.log(np.where(finite, np.exp(x - m), 0.0).sum())
+
+
+def causal_lse(Q, K):
+    """Row log-sum-exp of the prompt's causal attention: lse_i = ln sum_{j <= i}
+    exp(q_i . k_j / sqrt(d)) for Q [L, d], K [L, d].  Returns [L] in fp64, one row at a
+    time."""
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    d = Q.shape[-1]
+    return np.array([log_sum_exp(K[: i + 1] @ Q[i] / np.sqrt(d)) for i in range(Q.shape[0])])

@@ -57,6 +57,35 @@ def window_votes(q_unit, K):
     return v
 
 
+def votes_from_lse(q_unit, K, lse_unit):
+    """Steps 1 and 2 with each window row's softmax normaliser given: row (g, r) at
+    position i = L - Wq + r adds exp(q . k_j / sqrt(d) - lse_unit[g, i]) to v_j for every
+    key j <= i.  With lse_unit the rows' own log-sum-exp (attention.causal_lse) each
+    term is the row's softmax weight and v equals window_votes; another lse scales each
+    row's contribution by exp(true lse - given lse).  A non-finite entry makes its row
+    add nothing.
+
+    q_unit: [G, Wq, d]; K: [L, d]; lse_unit: [G, L] (positions L-Wq..L-1 are read).
+    Returns v [L] in fp64.
+    """
+    q_unit = np.asarray(q_unit, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    lse_unit = np.asarray(lse_unit, dtype=np.float64)
+    G, Wq, d = q_unit.shape
+    L = K.shape[0]
+    if Wq > L:
+        raise ValueError("more window queries than prompt positions")
+    v = np.zeros(L, dtype=np.float64)
+    for g in range(G):
+        for r in range(Wq):
+            pos = L - Wq + r
+            lse = lse_unit[g, pos]
+            if not np.isfinite(lse):
+                continue
+            v[: pos + 1] += np.exp(K[: pos + 1] @ q_unit[g, r] / np.sqrt(d) - lse)
+    return v
+
+
 def max_pool_1d(v, kernel):
     """Step 3: u_j = max of v over the positions within (kernel-1)/2 of j.
 

@@ -1,6 +1,7 @@
 """Pins of the oracle's softmax attention against closed forms and invariants."""
 
 import numpy as np
+import pytest
 
 from oracle import attention as A
 
@@ -80,3 +81,37 @@ def test_causal_prefill_closed_forms_and_second_route():
     for i in (0, 7, L - 1):
         vis = np.arange(L) <= i
         np.testing.assert_allclose(O[i], A.attend_masked(Q[i], K, V, vis), rtol=1e-12, atol=1e-14)
+
+
+def test_log_sum_exp_hand_worked_rows():
+    # d = 4 (scale 1/2), q = (2, 0, 0, 0) and k_j = (x_j, ...) give logits x_j:
+    # x = (0, ln 2, ln 5) -> row 0: ln 1, row 1: ln (1 + 2) = ln 3, row 2: ln (1 + 2 + 5) = ln 8.
+    x = np.array([0.0, np.log(2.0), np.log(5.0)])
+    Q = np.tile(np.array([2.0, 0, 0, 0]), (3, 1))
+    K = np.zeros((3, 4))
+    K[:, 0] = x
+    K[:, 1:] = 7.0  # orthogonal to q: no effect
+    np.testing.assert_allclose(A.causal_lse(Q, K), np.log([1.0, 3.0, 8.0]), rtol=0, atol=1e-15)
+
+
+def test_lse_of_zero_queries_is_log_of_row_length():
+    rng = np.random.default_rng(11)
+    K = rng.normal(size=(9, 8)) * 5
+    np.testing.assert_allclose(A.causal_lse(np.zeros((9, 8)), K), np.log(np.arange(1, 10)),
+                               rtol=0, atol=1e-14)
+
+
+def test_lse_normalises_the_attention_weights_and_matches_scipy():
+    scipy_special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(12)
+    L, d = 40, 16
+    Q, K = rng.normal(size=(L, d)) * 3, rng.normal(size=(L, d)) * 3
+    lse = A.causal_lse(Q, K)
+    for i in (0, 1, 17, L - 1):
+        logits = K[: i + 1] @ Q[i] / np.sqrt(d)
+        np.testing.assert_allclose(np.exp(logits - lse[i]), A.attention_weights(Q[i], K[: i + 1]),
+                                   rtol=1e-12)
+        np.testing.assert_allclose(lse[i], scipy_special.logsumexp(logits), rtol=1e-14)
+    # -inf logits add nothing; huge logits stay finite
+    assert A.log_sum_exp([-np.inf, 0.0]) == 0.0
+    np.testing.assert_allclose(A.log_sum_exp([1000.0, 1000.0]), 1000.0 + np.log(2.0), rtol=1e-15)

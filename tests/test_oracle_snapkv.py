@@ -176,3 +176,43 @@ def test_select_positions_with_average_pooling():
     assert list(S.select_positions(votes, 14, 2, 3, 3, pool="avg")) == [8, 12, 13]
     with pytest.raises(ValueError):
         S.select_positions(votes, 14, 2, 3, 3, pool="median")
+
+
+def test_votes_from_true_lse_equal_window_votes():
+    # A second route to steps 1-2: with each row's own log-sum-exp the terms are the rows'
+    # softmax weights (GQA group of 3, window 5, prefix 12).
+    rng = np.random.default_rng(21)
+    G, Wq, L, d = 3, 5, 17, 8
+    q_unit = rng.normal(size=(G, Wq, d)) * 2
+    K = rng.normal(size=(L, d)) * 2
+    lse = np.full((G, L), np.nan)
+    for g in range(G):
+        Qfull = np.zeros((L, d))
+        Qfull[L - Wq:] = q_unit[g]
+        lse[g, L - Wq:] = A.causal_lse(Qfull, K)[L - Wq:]
+    np.testing.assert_allclose(S.votes_from_lse(q_unit, K, lse), S.window_votes(q_unit, K),
+                               rtol=1e-13)
+
+
+def test_votes_from_shifted_lse_scale_per_row():
+    # lse + c on one row scales that row's contribution by e^-c; a non-finite lse drops it.
+    rng = np.random.default_rng(22)
+    G, Wq, L, d = 2, 3, 9, 4
+    q_unit = rng.normal(size=(G, Wq, d))
+    K = rng.normal(size=(L, d))
+    lse = rng.normal(size=(G, L))
+    base = S.votes_from_lse(q_unit, K, lse)
+    one_row = np.zeros((G, Wq, d))
+    one_row[1, 2] = q_unit[1, 2]
+    masked = np.full((G, L), -np.inf)
+    masked[1, L - 1] = lse[1, L - 1]
+    row_only = S.votes_from_lse(one_row, K, masked)
+    assert np.all(row_only > 0)                # only row (1, 2) at position L-1 adds
+    shifted = lse.copy()
+    shifted[1, L - 1] += np.log(4.0)
+    np.testing.assert_allclose(S.votes_from_lse(q_unit, K, shifted), base - 0.75 * row_only,
+                               rtol=1e-12)
+    dropped = lse.copy()
+    dropped[1, L - 1] = np.inf
+    np.testing.assert_allclose(S.votes_from_lse(q_unit, K, dropped), base - row_only, rtol=1e-12,
+                               atol=1e-15)
