@@ -72,6 +72,9 @@ _SIGS = {
                                      _P, ctypes.c_size_t, _P]),
     "snapkv_prefill_attention": (ctypes.c_int, [ctypes.POINTER(SnapKVParams), _P, _P, _P, _P, _P,
                                                 _P]),
+    "prefill_attention_lse": (ctypes.c_int, [ctypes.POINTER(SnapKVParams), _P, _P, _P, _P, _P,
+                                             _P]),
+    "snapkv_votes_from_lse": (ctypes.c_int, [ctypes.POINTER(SnapKVParams), _P, _P, _P, _P, _P]),
     "compressed_decode_attn_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(DecodeParams)]),
     "compressed_decode_attn": (ctypes.c_int, [ctypes.POINTER(DecodeParams), _P, _P, _P, _P, _P, _P,
                                               _P, _P, _P, ctypes.c_size_t, _P]),
@@ -82,6 +85,9 @@ _SIGS = {
     "h2o_step_ctas_per_unit": (ctypes.c_int32, [ctypes.POINTER(H2OParams)]),
     "h2o_prefill": (ctypes.c_int, [ctypes.POINTER(H2OParams), ctypes.c_int32, _P, _P, _P,
                                    ctypes.POINTER(H2OStateC), _P, ctypes.c_size_t, _P]),
+    "h2o_prefill_from_votes": (ctypes.c_int, [ctypes.POINTER(H2OParams), ctypes.c_int32, _P, _P,
+                                              _P, ctypes.POINTER(H2OStateC), _P, ctypes.c_size_t,
+                                              _P]),
     "h2o_decode_step": (ctypes.c_int, [ctypes.POINTER(H2OParams), _P, _P, _P,
                                        ctypes.POINTER(H2OStateC), ctypes.c_int32, _P, _P, _P]),
     "sink_window_append": (ctypes.c_int, [ctypes.POINTER(SinkParams), _P, _P, _P, _P, _P,
@@ -278,6 +284,52 @@ def snapkv_prefill_attention(q, k, v, *, window=None, out=None, votes_out=None, 
     return out, votes_out
 
 
+def prefill_attention_lse(q, k, v, *, out=None, lse_out=None, stream=None):
+    """Causal self-attention of the prompt, q [Ly,B,Hq,L,D], k, v [Ly,B,Hkv,L,D] -> out
+    [Ly,B,Hq,L,D] and each row's log-sum-exp lse [Ly,B,Hq,L] fp32 (natural log of the
+    softmax normaliser).  Returns (out, lse)."""
+    bf = torch.bfloat16
+    _need(q, "q", bf)
+    _need(k, "k", bf)
+    _need(v, "v", bf, k.shape)
+    Ly, B, Hkv, L, D = k.shape
+    if q.shape[:2] != k.shape[:2] or q.shape[3:] != k.shape[3:] or q.shape[2] % Hkv:
+        raise ValueError("q %s and k %s disagree" % (tuple(q.shape), tuple(k.shape)))
+    if out is None:
+        out = torch.empty_like(q)
+    if lse_out is None:
+        lse_out = torch.empty(q.shape[:4], dtype=torch.float32, device=q.device)
+    _need(out, "out", bf, q.shape)
+    _need(lse_out, "lse_out", torch.float32, tuple(q.shape[:4]))
+    p = SnapKVParams(Ly, B, q.shape[2], Hkv, D, L, 1, 0, 1, 1, 1, 0)
+    code = lib().prefill_attention_lse(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                       _ptr(lse_out), _stream(stream))
+    _check(code, "prefill_attention_lse")
+    return out, lse_out
+
+
+def snapkv_votes_from_lse(q_win, k, lse, *, votes_out=None, stream=None):
+    """Votes of the Wq window queries q_win [Ly,B,Hq,Wq,D] over k [Ly,B,Hkv,L,D], given every
+    row's log-sum-exp lse [Ly,B,Hq,L] (prefill_attention_lse's): fp32 [Ly,B,Hkv,L], the
+    votes snapkv_compress forms (H2O's initial scores when Wq = L)."""
+    bf = torch.bfloat16
+    _need(q_win, "q_win", bf)
+    _need(k, "k", bf)
+    Ly, B, Hkv, L, D = k.shape
+    Hq, Wq = q_win.shape[2], q_win.shape[3]
+    if q_win.shape[:2] != k.shape[:2] or q_win.shape[4] != D or Hq % Hkv or Wq > L:
+        raise ValueError("q_win %s and k %s disagree" % (tuple(q_win.shape), tuple(k.shape)))
+    _need(lse, "lse", torch.float32, (Ly, B, Hq, L))
+    if votes_out is None:
+        votes_out = torch.empty((Ly, B, Hkv, L), dtype=torch.float32, device=k.device)
+    _need(votes_out, "votes_out", torch.float32, (Ly, B, Hkv, L))
+    p = SnapKVParams(Ly, B, Hq, Hkv, D, L, Wq, 0, 1, 1, 1, 0)
+    code = lib().snapkv_votes_from_lse(ctypes.byref(p), _ptr(q_win), _ptr(k), _ptr(lse),
+                                       _ptr(votes_out), _stream(stream))
+    _check(code, "snapkv_votes_from_lse")
+    return votes_out
+
+
 def snapkv_select(votes, k, v, *, keep_window, pool_kernel, budget, cap=None, pool_avg=False,
                   stream=None):
     """Steps 3-4 of snapkv_compress (pool, top-k, gather) from given votes [Ly,B,Hkv,L]
@@ -435,6 +487,29 @@ def h2o_prefill(q, k, v, *, n_heavy, n_recent, state=None, workspace_buf=None, s
     code = lib().h2o_prefill(ctypes.byref(p), L, _ptr(q), _ptr(k), _ptr(v), ctypes.byref(st),
                              _ptr(ws), ws.numel(), _stream(stream))
     _check(code, "h2o_prefill")
+    return state
+
+
+def h2o_prefill_from_votes(votes, k, v, *, n_q_heads, n_heavy, n_recent, state=None,
+                           workspace_buf=None, stream=None):
+    """h2o_prefill from given initial scores votes [Ly,B,Hkv,L] fp32 (e.g.
+    snapkv_votes_from_lse over every prompt query); k, v [Ly,B,Hkv,L,D].  Returns an
+    H2OState."""
+    bf = torch.bfloat16
+    _need(k, "k", bf)
+    _need(v, "v", bf, k.shape)
+    Ly, B, Hkv, L, D = k.shape
+    _need(votes, "votes", torch.float32, (Ly, B, Hkv, L))
+    if state is None:
+        state = H2OState(Ly, B, Hkv, D, n_heavy, n_recent, k.device)
+    p = H2OParams(Ly, B, n_q_heads, Hkv, D, n_heavy, n_recent)
+    nbytes = lib().h2o_prefill_workspace_bytes(ctypes.byref(p), L)
+    ws = workspace(nbytes, k.device, "snapkv") if workspace_buf is None else workspace_buf
+    st = state.c_struct()
+    code = lib().h2o_prefill_from_votes(ctypes.byref(p), L, _ptr(votes), _ptr(k), _ptr(v),
+                                        ctypes.byref(st), _ptr(ws), ws.numel(),
+                                        _stream(stream))
+    _check(code, "h2o_prefill_from_votes")
     return state
 
 

@@ -293,6 +293,108 @@ kvc_status device_check(kvc_stream_t stream) {
   return get_ctx(stream, &c);
 }
 
+// The causal prefill attention with optional votes of the last n_query rows and optional
+// per-row log-sum-exp.
+kvc_status prefill_call(const kvc_snapkv_params *p, const void *q, const void *k, const void *v,
+                        void *o_out, float *votes_out, float *lse_out, kvc_stream_t stream) {
+  ensure_encode();
+  Ctx c;
+  kvc_status st = get_ctx(stream, &c);
+  if (st != KVC_OK) return st;
+  if (!p) return KVC_ERR_NULL;
+  if (!common_heads_ok(p->n_layers, p->batch, p->n_q_heads, p->n_kv_heads, p->head_dim) ||
+      p->prompt_len < 1 || (votes_out && (p->n_query < 1 || p->n_query > p->prompt_len)))
+    return KVC_ERR_SHAPE;
+  const long long uq = (long long)p->n_layers * p->batch * p->n_q_heads;
+  if (uq * p->prompt_len > kMaxRows) return KVC_ERR_SHAPE;
+  if (!q || !k || !v || !o_out) return KVC_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_out) ||
+      (votes_out && !aligned4(votes_out)) || (lse_out && !aligned4(lse_out)))
+    return KVC_ERR_ALIGN;
+  if (!g_encode) return KVC_ERR_CUDA;
+  PrefillArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o_out;
+  a.votes = votes_out;
+  a.lse = lse_out;
+  a.units_q = (int)uq;
+  a.G = p->n_q_heads / p->n_kv_heads;
+  a.L = p->prompt_len;
+  a.D = p->head_dim;
+  a.Wq = votes_out ? p->n_query : 1;
+  return cuda_status(launch_prefill(c, a));
+}
+
+
+// h2o_prefill from the prompt's queries (q) or from column sums computed elsewhere (votes).
+kvc_status h2o_prefill_call(const kvc_h2o_params *p, int32_t prompt_len, const void *q,
+                            const float *votes, const void *k, const void *v,
+                            const kvc_h2o_state *st, void *workspace, size_t workspace_bytes,
+                            kvc_stream_t stream) {
+  ensure_encode();
+  if (!p || !st) return KVC_ERR_NULL;
+  if (p->n_heavy < 0 || p->n_recent < 1) return KVC_ERR_SHAPE;
+  if (!st->k || !st->v || !st->score || !st->pos || !st->n_used || !st->free_slot)
+    return KVC_ERR_NULL;
+  if (!aligned4(st->n_used) || !aligned4(st->free_slot)) return KVC_ERR_ALIGN;
+  kvc_snapkv_params s;
+  s.n_layers = p->n_layers;
+  s.batch = p->batch;
+  s.n_q_heads = p->n_q_heads;
+  s.n_kv_heads = p->n_kv_heads;
+  s.head_dim = p->head_dim;
+  s.prompt_len = prompt_len;
+  s.n_query = prompt_len;
+  s.keep_window = p->n_recent;
+  s.pool_kernel = 1;
+  s.pool_avg = 0;
+  s.budget = p->n_heavy + p->n_recent;
+  s.cap = p->n_heavy + p->n_recent + 1;
+  kvc_status r = run_snapkv(&s, q, k, v, st->k, st->v, st->pos, st->n_used, nullptr, st->score,
+                            workspace, workspace_bytes, stream, votes);
+  if (r != KVC_OK) return r;
+  Ctx c;
+  r = get_ctx(stream, &c);
+  if (r != KVC_OK) return r;
+  const long long units = (long long)p->n_layers * p->batch * p->n_kv_heads;
+  return cuda_status(
+      launch_h2o_init_state(c, st->pos, st->n_used, st->free_slot, st->n_used, (int)units, s.cap));
+}
+
+// Step 2 of SnapKV (or H2O's column sums with n_query = L) from the rows' log-sum-exp.
+kvc_status votes_from_lse_call(const kvc_snapkv_params *p, const void *q_win, const void *k,
+                               const float *lse, float *votes_out, kvc_stream_t stream) {
+  ensure_encode();
+  Ctx c;
+  kvc_status st = get_ctx(stream, &c);
+  if (st != KVC_OK) return st;
+  if (!p) return KVC_ERR_NULL;
+  if (!common_heads_ok(p->n_layers, p->batch, p->n_q_heads, p->n_kv_heads, p->head_dim) ||
+      p->prompt_len < 1 || p->n_query < 1 || p->n_query > p->prompt_len)
+    return KVC_ERR_SHAPE;
+  const long long units = (long long)p->n_layers * p->batch * p->n_kv_heads;
+  const int G = p->n_q_heads / p->n_kv_heads;
+  if ((long long)G * p->n_query > kMaxRows || units * G * p->n_query > kMaxRows ||
+      units * G * p->prompt_len > kMaxRows)
+    return KVC_ERR_SHAPE;
+  if (!q_win || !k || !lse || !votes_out) return KVC_ERR_NULL;
+  if (!aligned16(q_win) || !aligned16(k) || !aligned4(lse) || !aligned4(votes_out))
+    return KVC_ERR_ALIGN;
+  if (!g_encode) return KVC_ERR_CUDA;
+  WindowVoteLseArgs a;
+  a.q = q_win;
+  a.k = k;
+  a.lse = lse;
+  a.units = (int)units;
+  a.L = p->prompt_len;
+  a.G = G;
+  a.Wq = p->n_query;
+  a.D = p->head_dim;
+  a.votes = votes_out;
+  return cuda_status(launch_window_vote_lse(c, a));
+}
 
 }  // namespace kvc
 
@@ -381,33 +483,20 @@ kvc_status snapkv_prefill_attention(const kvc_snapkv_params *p, const void *q, c
                                     const void *v, void *o_out, float *votes_out,
                                     kvc_stream_t stream) {
   const TraceRange trace_range("snapkv_prefill_attention");
-  ensure_encode();
-  Ctx c;
-  kvc_status st = get_ctx(stream, &c);
-  if (st != KVC_OK) return st;
-  if (!p) return KVC_ERR_NULL;
-  if (!common_heads_ok(p->n_layers, p->batch, p->n_q_heads, p->n_kv_heads, p->head_dim) ||
-      p->prompt_len < 1 || (votes_out && (p->n_query < 1 || p->n_query > p->prompt_len)))
-    return KVC_ERR_SHAPE;
-  const long long uq = (long long)p->n_layers * p->batch * p->n_q_heads;
-  if (uq * p->prompt_len > kMaxRows) return KVC_ERR_SHAPE;
-  if (!q || !k || !v || !o_out) return KVC_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_out) ||
-      (votes_out && !aligned4(votes_out)))
-    return KVC_ERR_ALIGN;
-  if (!g_encode) return KVC_ERR_CUDA;
-  PrefillArgs a;
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.o = o_out;
-  a.votes = votes_out;
-  a.units_q = (int)uq;
-  a.G = p->n_q_heads / p->n_kv_heads;
-  a.L = p->prompt_len;
-  a.D = p->head_dim;
-  a.Wq = p->n_query;
-  return cuda_status(launch_prefill(c, a));
+  return kvc::prefill_call(p, q, k, v, o_out, votes_out, nullptr, stream);
+}
+
+kvc_status prefill_attention_lse(const kvc_snapkv_params *p, const void *q, const void *k,
+                                 const void *v, void *o_out, float *lse_out, kvc_stream_t stream) {
+  const TraceRange trace_range("prefill_attention_lse");
+  if (!lse_out) return KVC_ERR_NULL;
+  return kvc::prefill_call(p, q, k, v, o_out, nullptr, lse_out, stream);
+}
+
+kvc_status snapkv_votes_from_lse(const kvc_snapkv_params *p, const void *q_win, const void *k,
+                                 const float *lse, float *votes_out, kvc_stream_t stream) {
+  const TraceRange trace_range("snapkv_votes_from_lse");
+  return kvc::votes_from_lse_call(p, q_win, k, lse, votes_out, stream);
 }
 
 size_t compressed_decode_attn_workspace_bytes(const kvc_decode_params *p) {
@@ -476,34 +565,19 @@ kvc_status h2o_prefill(const kvc_h2o_params *p, int32_t prompt_len, const void *
                        const void *v, const kvc_h2o_state *st, void *workspace,
                        size_t workspace_bytes, kvc_stream_t stream) {
   const TraceRange trace_range("h2o_prefill");
-  ensure_encode();
-  if (!p || !st) return KVC_ERR_NULL;
-  if (p->n_heavy < 0 || p->n_recent < 1) return KVC_ERR_SHAPE;
-  if (!st->k || !st->v || !st->score || !st->pos || !st->n_used || !st->free_slot)
-    return KVC_ERR_NULL;
-  if (!aligned4(st->n_used) || !aligned4(st->free_slot)) return KVC_ERR_ALIGN;
-  kvc_snapkv_params s;
-  s.n_layers = p->n_layers;
-  s.batch = p->batch;
-  s.n_q_heads = p->n_q_heads;
-  s.n_kv_heads = p->n_kv_heads;
-  s.head_dim = p->head_dim;
-  s.prompt_len = prompt_len;
-  s.n_query = prompt_len;
-  s.keep_window = p->n_recent;
-  s.pool_kernel = 1;
-  s.pool_avg = 0;
-  s.budget = p->n_heavy + p->n_recent;
-  s.cap = p->n_heavy + p->n_recent + 1;
-  kvc_status r = run_snapkv(&s, q, k, v, st->k, st->v, st->pos, st->n_used, nullptr, st->score,
-                            workspace, workspace_bytes, stream);
-  if (r != KVC_OK) return r;
-  Ctx c;
-  r = get_ctx(stream, &c);
-  if (r != KVC_OK) return r;
-  const long long units = (long long)p->n_layers * p->batch * p->n_kv_heads;
-  return cuda_status(
-      launch_h2o_init_state(c, st->pos, st->n_used, st->free_slot, st->n_used, (int)units, s.cap));
+  if (!q) return KVC_ERR_NULL;
+  return kvc::h2o_prefill_call(p, prompt_len, q, nullptr, k, v, st, workspace, workspace_bytes,
+                               stream);
+}
+
+kvc_status h2o_prefill_from_votes(const kvc_h2o_params *p, int32_t prompt_len,
+                                  const float *votes, const void *k, const void *v,
+                                  const kvc_h2o_state *st, void *workspace,
+                                  size_t workspace_bytes, kvc_stream_t stream) {
+  const TraceRange trace_range("h2o_prefill_from_votes");
+  if (!votes) return KVC_ERR_NULL;
+  return kvc::h2o_prefill_call(p, prompt_len, nullptr, votes, k, v, st, workspace,
+                               workspace_bytes, stream);
 }
 
 kvc_status h2o_decode_step(const kvc_h2o_params *p, const void *q, const void *k_new,

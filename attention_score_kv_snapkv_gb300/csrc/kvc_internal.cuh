@@ -371,6 +371,16 @@ bool plan_window_vote_tmem(int units, int L, int R, int Wq, int num_sms, WindowV
 cudaError_t launch_window_vote_tmem(const Ctx &c, const WindowVoteArgs &a,
                                     const WindowVotePlan &pl);
 
+// window_vote_lse.cu: step 2 when each voting row's log-sum-exp is already known.
+struct WindowVoteLseArgs {
+  const void *q;      // [U * R, D] bf16, R = G * Wq rows per unit
+  const void *k;      // [U * L, D] bf16
+  const float *lse;   // [U, G, L] fp32 natural-log log-sum-exp of every prompt row
+  int units, L, G, Wq, D;
+  float *votes;       // [U, L] fp32 (zeroed here when several row tiles add into it)
+};
+cudaError_t launch_window_vote_lse(const Ctx &c, const WindowVoteLseArgs &a);
+
 // select.cu: steps 3-4 (pool + top-k + gather).
 struct SelectArgs {
   const float *votes;   // [U, L]
@@ -450,5 +460,8 @@ kvc_status decode_call(const kvc_decode_params *p, const void *q, const void *k_
                        kvc_stream_t stream, bool clear_counters);
 // kvc_api.cu: KVC_OK if the current device is supported (sm_103), else its error.
 kvc_status device_check(kvc_stream_t stream);
+// kvc_api.cu: the causal prefill attention with optional votes and per-row log-sum-exp.
+kvc_status prefill_call(const kvc_snapkv_params *p, const void *q, const void *k, const void *v,
+                        void *o_out, float *votes_out, float *lse_out, kvc_stream_t stream);
 
 }  // namespace kvc

@@ -75,6 +75,7 @@ struct PreP {
   const __nv_bfloat16 *q;  // [Uq, L, D]
   __nv_bfloat16 *o;        // [Uq, L, D]
   float *votes;            // [Ukv, L] (zeroed by the launcher) or null
+  float *lse;              // [Uq, L] or null: natural-log log-sum-exp of each row's scores
   int L, G, Wq, uq, nqt;   // uq = query-head units, nqt = query tiles per head
   float c;                 // log2(e) / sqrt(D)
   uint32_t *status;
@@ -523,7 +524,10 @@ __global__ void __launch_bounds__(NTH, 1) prefill_kernel(const __grid_constant__
         }
         ++pc;
       }
-      // the job's output rows: O / l in bf16, then O is free for the next job
+      // the job's output rows: O / l in bf16, then O is free for the next job; and the
+      // row's log-sum-exp, ln 2 (m + log2 l) (m and l are in the log2 domain of s c)
+      if (ok && valid && p.lse)
+        p.lse[(size_t)J.uq * p.L + row] = l > 0.f ? 0.6931471805599453f * (m + lg2(l)) : -INFINITY;
       ok = __all_sync(0xffffffffu, ok && ab.wait(bar + B_PDONE, (pc - 1) & 1));
       if (ok) {
         tc_fence_after();
@@ -593,6 +597,7 @@ cudaError_t launch_prefill(const Ctx &c, const PrefillArgs &a) {
   p.q = reinterpret_cast<const __nv_bfloat16 *>(a.q);
   p.o = reinterpret_cast<__nv_bfloat16 *>(a.o);
   p.votes = a.votes;
+  p.lse = a.lse;
   p.L = a.L;
   p.G = a.G;
   p.Wq = a.Wq;

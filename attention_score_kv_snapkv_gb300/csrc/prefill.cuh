@@ -9,6 +9,7 @@ struct PrefillArgs {
   const void *k, *v;  // [Ukv, L, D] bf16, Ukv = Uq / G
   void *o;            // [Uq, L, D] bf16 output
   float *votes;       // [Ukv, L] fp32 or null (zeroed here before the launch)
+  float *lse;         // [Uq, L] fp32 or null: each row's log-sum-exp of its causal scores
   int units_q, G, L, D, Wq;
 };
 cudaError_t launch_prefill(const Ctx &c, const PrefillArgs &a);

@@ -655,6 +655,84 @@ def measure_prefill(kvc, WL, dev, tf_peak, layers=2, reps=3):
             "device_status": status}
 
 
+def measure_lse_route(kvc, WL, dev, tf_peak, hbm_peak, layers=2, reps=3):
+    """The scores through the rows' log-sum-exp: prefill_attention_lse, then
+    snapkv_votes_from_lse (one pass over the keys) and the selection, against the plain
+    prefill followed by the direct route (snapkv_compress / h2o_prefill).  SnapKV on
+    `layers` layers of the Mistral-7B-shaped prompt; H2O on one layer of the OPT-6.7B-shaped
+    prompt (every query votes)."""
+    import torch
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    w = WL.MISTRAL
+    x = WL.snapkv_prompt(w, WL.seed_of(2, 7), dev, layers=layers, full_queries=True)
+    Qf, K, V, Qw = x["Q_full"], x["K"], x["V"], x["Q_win"]
+    out = torch.empty_like(Qf)
+    lse = torch.empty(Qf.shape[:4], dtype=torch.float32, device=dev)
+    votes = torch.empty((layers, w.batch, w.kv_heads, w.prompt_len), dtype=torch.float32, device=dev)
+    kw = dict(keep_window=w.window, pool_kernel=w.pool_kernel, budget=w.budget, cap=w.budget)
+    t_plain = timed(lambda: kvc.snapkv_prefill_attention(Qf, K, V, out=out))
+    t_lse = timed(lambda: kvc.prefill_attention_lse(Qf, K, V, out=out, lse_out=lse))
+    t_vfl = timed(lambda: kvc.snapkv_votes_from_lse(Qw, K, lse, votes_out=votes))
+    t_select = timed(lambda: kvc.snapkv_select(votes, K, V, **kw))
+    t_compress = timed(lambda: kvc.snapkv_compress(Qw, K, V, **kw))
+    L, Wn = w.prompt_len, w.window
+    # algorithmic bytes of the vote pass: K once, the window queries, their lse, the votes
+    vfl_bytes = layers * w.batch * (w.kv_heads * L * w.head_dim * 2 + w.q_heads * Wn * w.head_dim * 2
+                                    + w.q_heads * Wn * 4 + w.kv_heads * L * 4)
+    snap = {"workload": "mistral7b-b2-L16384-gqa32x8-d128, %d layers" % layers,
+            "prefill_ms_per_layer": t_plain / layers,
+            "prefill_lse_ms_per_layer": t_lse / layers,
+            "votes_from_lse_ms_per_layer": t_vfl / layers,
+            "votes_from_lse_GBps": vfl_bytes / (t_vfl / 1e3) / 1e9,
+            "votes_from_lse_frac_of_hbm_peak": vfl_bytes / (t_vfl / 1e3) / 1e9 / hbm_peak,
+            "select_ms_per_layer": t_select / layers,
+            "compress_ms_per_layer": t_compress / layers,
+            "lse_route_ms_per_layer": (t_lse + t_vfl + t_select) / layers,
+            "direct_route_ms_per_layer": (t_plain + t_compress) / layers}
+    del x, Qf, K, V, Qw, out, lse, votes
+    torch.cuda.empty_cache()
+
+    w = WL.H2O_OPT
+    Q, K, V = WL.h2o_prompt_layer(w, 0, WL.seed_of(4), dev)
+    Q, K, V = Q[None], K[None], V[None]
+    out = torch.empty_like(Q)
+    lse = torch.empty(Q.shape[:4], dtype=torch.float32, device=dev)
+    scores = torch.empty((1, w.batch, w.kv_heads, w.prompt_len), dtype=torch.float32, device=dev)
+    st = kvc.H2OState(1, w.batch, w.kv_heads, w.head_dim, w.n_heavy, w.n_recent, dev)
+    hk = dict(n_heavy=w.n_heavy, n_recent=w.n_recent, state=st)
+    t_plain = timed(lambda: kvc.snapkv_prefill_attention(Q, K, V, out=out))
+    t_lse = timed(lambda: kvc.prefill_attention_lse(Q, K, V, out=out, lse_out=lse))
+    t_vfl = timed(lambda: kvc.snapkv_votes_from_lse(Q, K, lse, votes_out=scores))
+    t_cut = timed(lambda: kvc.h2o_prefill_from_votes(scores, K, V, n_q_heads=w.q_heads, **hk))
+    t_direct = timed(lambda: kvc.h2o_prefill(Q, K, V, **hk))
+    status = kvc.kvc_device_status()
+    Lp = w.prompt_len
+    qk_flops = 2.0 * w.batch * w.q_heads * Lp * (Lp + 1) / 2 * w.head_dim
+    h2o = {"workload": w.name + ", 1 layer",
+           "prefill_ms": t_plain, "prefill_lse_ms": t_lse,
+           "scores_from_lse_ms": t_vfl,
+           "scores_from_lse_causal_qk_TFLOPs": qk_flops / (t_vfl / 1e3) / 1e12,
+           "scores_from_lse_frac_of_bf16_peak": qk_flops / (t_vfl / 1e3) / 1e12 / tf_peak,
+           "cut_from_scores_ms": t_cut,
+           "h2o_prefill_direct_ms": t_direct,
+           "lse_route_ms": t_lse + t_vfl + t_cut,
+           "direct_route_ms": t_plain + t_direct}
+    del Q, K, V, out, lse, scores, st
+    torch.cuda.empty_cache()
+    return {"snapkv": snap, "h2o": h2o, "device_status": status}
+
+
 def measure_stream(kvc, WL, dev, hbm_peak, steps=256, n_sink=None, ring=None):
     """StreamingLLM on Llama-2-13B shapes (batch 16, 40 layers, 40 MHA heads, 4 sinks +
     2044-token ring, or the given sink count and ring): fill the cache, then steady-state
@@ -760,7 +838,11 @@ def run_profile_driver(args):
             of the StreamingLLM (Llama-2-13B) shape, fill + 4 steady-state steps;
     long:   three compressions of two layers of the long-context shape (L = 131072);
     prefill: three prefill attentions with votes on one layer, batch 1 of the
-            Mistral-7B-shaped prompt (32 query heads, 8 KV heads, L = 16384, D = 128)."""
+            Mistral-7B-shaped prompt (32 query heads, 8 KV heads, L = 16384, D = 128);
+    lse:    the log-sum-exp route: one prefill_attention_lse and three
+            snapkv_votes_from_lse on four layers of the Mistral-7B-shaped prompt, then the
+            same on one layer of the OPT-6.7B-shaped H2O prompt at batch 16 (every query
+            votes)."""
     import torch
 
     import attention_score_kv_snapkv_gb300 as kvc
@@ -782,6 +864,23 @@ def run_profile_driver(args):
         for _ in range(3):
             kvc.snapkv_prefill_attention(x["Q_full"], x["K"], x["V"], window=w.window, out=out,
                                          votes_out=votes)
+    elif args.profile == "lse":
+        import dataclasses
+        w = WL.MISTRAL
+        x = WL.snapkv_prompt(w, 5, dev, layers=4, full_queries=True)
+        out, lse = kvc.prefill_attention_lse(x["Q_full"], x["K"], x["V"])
+        votes = torch.empty((4, w.batch, w.kv_heads, w.prompt_len), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            kvc.snapkv_votes_from_lse(x["Q_win"], x["K"], lse, votes_out=votes)
+        torch.cuda.synchronize()
+        del x, out, lse, votes
+        torch.cuda.empty_cache()
+        w = dataclasses.replace(WL.H2O_OPT, batch=16)
+        Q, K, V = WL.h2o_prompt_layer(w, 0, WL.seed_of(4), dev)
+        out, lse = kvc.prefill_attention_lse(Q[None], K[None], V[None])
+        del out
+        for _ in range(3):
+            kvc.snapkv_votes_from_lse(Q[None], K[None], lse)
     elif args.profile == "h2o-split":
         # one layer of the H2O cache at 20% of a 131072-token context: 32 units of 26215
         # slots, each split over several CTAs; four steps
@@ -1060,6 +1159,7 @@ def run_ours(args):
                        "mistral_pool_ablation": pools,
                        "long_context": measure_long(kvc, WL, dev, hbm_peak),
                        "prefill_with_votes": measure_prefill(kvc, WL, dev, tf_peak),
+                       "lse_route": measure_lse_route(kvc, WL, dev, tf_peak, hbm_peak),
                        "h2o": measure_h2o(kvc, WL, dev, hbm_peak),
                        # the other reading of the 20% budget: 20% of the total length
                        # (prompt 2048 + 2048 generated), 409 heavy + 409 recent
@@ -1094,7 +1194,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-aux", action="store_true",
                     help="skip the long-context, H2O and streaming measurements")
-    ap.add_argument("--profile", choices=["decode", "aux", "long", "prefill", "h2d", "h2o-split"],
+    ap.add_argument("--profile", choices=["decode", "aux", "long", "prefill", "h2d", "h2o-split",
+                                          "lse"],
                     default=None,
                     help="run a short fixed workload for an ncu capture instead of the bench "
                          "(h2d: measure the host-link copy rates)")

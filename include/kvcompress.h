@@ -178,6 +178,36 @@ kvc_status snapkv_prefill_attention(const kvc_snapkv_params *p, const void *q, c
                                     const void *v, void *o_out, float *votes_out,
                                     kvc_stream_t stream);
 
+/* The prompt's causal self-attention (as snapkv_prefill_attention without votes) that also
+ * writes each row's log-sum-exp: lse_out[.., i] = ln sum_{j <= i} exp(q_i . k_j / sqrt(D)),
+ * the normaliser of the row's softmax (SnapKV article, 処理の流れ step 1, and the H2O
+ * article, 処理の流れ: both scores are rows of this softmax).  With it,
+ * snapkv_votes_from_lse forms the SnapKV votes, or H2O's initial scores, in one pass over
+ * the keys.  Uses n_layers, batch, n_q_heads, n_kv_heads, head_dim and prompt_len of p.
+ * Inputs (dev, bf16): q [Ly,B,Hq,L,D], k, v [Ly,B,Hkv,L,D].  Outputs (dev): o_out bf16
+ * [Ly,B,Hq,L,D]; lse_out fp32 [Ly,B,Hq,L] (natural logarithm; must not be NULL).
+ * Needs no workspace.  Errors: as snapkv_prefill_attention. */
+kvc_status prefill_attention_lse(const kvc_snapkv_params *p, const void *q, const void *k,
+                                 const void *v, void *o_out, float *lse_out,
+                                 kvc_stream_t stream);
+
+/* Step 2 of snapkv_compress (the vote) when every voting row's softmax normaliser is
+ * known (prefill_attention_lse): v_j = sum over the G * Wq voting rows i that see key j
+ * of exp(q_i . k_j / sqrt(D) - lse_i), fp32, every position j of every unit.  These are
+ * snapkv_compress's votes_out up to fp32 rounding when lse is the rows' own log-sum-exp;
+ * feed them to snapkv_select (SnapKV) or h2o_prefill_from_votes (n_query = L: H2O's
+ * initial cumulative scores).  One pass over the keys, no statistics pass.
+ * Uses n_layers, batch, n_q_heads, n_kv_heads, head_dim, prompt_len and n_query of p.
+ * Inputs (dev): q_win bf16 [Ly,B,Hq,Wq,D] (the trailing Wq queries of every head);
+ * k bf16 [Ly,B,Hkv,L,D]; lse fp32 [Ly,B,Hq,L] (only positions L-Wq..L-1 are read; a
+ * non-finite entry makes its row add nothing).  Output: votes_out fp32 [Ly,B,Hkv,L].
+ * When G * Wq > 128 several row tiles add into a key's vote with atomic adds, so the
+ * order of the additions, and the last bits, can vary between calls.
+ * Needs no workspace.  Errors: KVC_ERR_NULL, KVC_ERR_SHAPE, KVC_ERR_ALIGN, KVC_ERR_CUDA,
+ * KVC_ERR_UNSUPPORTED. */
+kvc_status snapkv_votes_from_lse(const kvc_snapkv_params *p, const void *q_win, const void *k,
+                                 const float *lse, float *votes_out, kvc_stream_t stream);
+
 /* ------------------------------------------------------------------------------ */
 /* Decode attention over a compact (SnapKV) or ring (StreamingLLM) cache           */
 /* ([SnapKV] 推論方法: decoding reads only the compressed cache; [StreamingLLM]       */
@@ -274,6 +304,15 @@ size_t h2o_prefill_workspace_bytes(const kvc_h2o_params *p, int32_t prompt_len);
 kvc_status h2o_prefill(const kvc_h2o_params *p, int32_t prompt_len, const void *q,
                        const void *k, const void *v, const kvc_h2o_state *st,
                        void *workspace, size_t workspace_bytes, kvc_stream_t stream);
+
+/* h2o_prefill from column sums computed elsewhere: votes fp32 [Ly,B,Hkv,L] (dev, read
+ * only) hold each position's initial cumulative score, e.g. snapkv_votes_from_lse with
+ * n_query = prompt_len.  The cut, the gathered state and the errors are those of
+ * h2o_prefill (h2o_prefill_workspace_bytes(p, prompt_len) bytes of workspace suffice). */
+kvc_status h2o_prefill_from_votes(const kvc_h2o_params *p, int32_t prompt_len,
+                                  const float *votes, const void *k, const void *v,
+                                  const kvc_h2o_state *st, void *workspace,
+                                  size_t workspace_bytes, kvc_stream_t stream);
 
 /* One decode step of token position t for every unit: write (k_new, v_new) into
  * free_slot, attend over every live entry (the new one included) giving out, add each
