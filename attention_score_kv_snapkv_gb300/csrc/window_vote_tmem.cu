@@ -411,7 +411,8 @@ __global__ void __launch_bounds__(Roles<NCH>::NTHREADS, 1)
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
-      int kit = 0, it = 0, last_bar = -1, last_par = 0, qcnt[NQ] = {};
+      int kit = 0, last_bar = -1, last_par = 0, qcnt[NQ] = {};
+      int b = 0, bph = 0;  // the tile's buffer and its use parity (no division per tile)
       bool ok = true;
       for (int k = 0; k < njobs && ok; ++k) {
         const Job J = job_geo(p, job_of(k), xg);
@@ -426,12 +427,10 @@ __global__ void __launch_bounds__(Roles<NCH>::NTHREADS, 1)
         for (int i = 0; i < n; ++i) {
           const int s = kit % NSTAGE, kuse = kit / NSTAGE;
           ++kit;
-          const int b = it % NB, use = it / NB;
-          ++it;
           // the stage's parity identifies the tile only once the producer has started it
           if (!wait_tag(tag + s, kit - 1, ab)) { ok = false; break; }
           if (!ab.wait(ctl + C_KFULL + 8 * s, kuse & 1)) { ok = false; break; }
-          if (!ab.wait(ctl + C_TFREE + 8 * b, (use & 1) ^ 1)) { ok = false; break; }
+          if (!ab.wait(ctl + C_TFREE + 8 * b, bph ^ 1)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d = tmem + (uint32_t)(b * QR);
           const uint64_t kd = sdesc_k128(sK + s * G::TILE_BYTES);
@@ -447,7 +446,11 @@ __global__ void __launch_bounds__(Roles<NCH>::NTHREADS, 1)
           umma_commit(ctl + C_KEMPTY + 8 * s);
           umma_commit(ctl + C_SFULL + 8 * b);
           last_bar = b;
-          last_par = use & 1;
+          last_par = bph;
+          if (++b == NB) {
+            b = 0;
+            bph ^= 1;
+          }
         }
         if (!ok) break;
         umma_commit(ctl + C_QEMPTY + 8 * qb);  // done with the Q tile
@@ -469,6 +472,7 @@ __global__ void __launch_bounds__(Roles<NCH>::NTHREADS, 1)
 #pragma unroll
     for (int r = 0; r < 32; ++r) acc[r] = 0.f;
     int it = 0;
+    int sb_b = 0, sb_ph = 0;  // the tile's buffer and its use parity
     bool ok = true;
     for (int k = 0; k < njobs; ++k) {
       const int j = job_of(k);
@@ -479,8 +483,13 @@ __global__ void __launch_bounds__(Roles<NCH>::NTHREADS, 1)
       rp[lane] = row_pos(p, J, row0 + lane);  // read only by this warp
       __syncwarp();
       for (int i = 0; i < n; ++i, ++it) {
-        const int b = it % NB;
-        const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_SFULL + 8 * b, (it / NB) & 1));
+        const int b = sb_b;
+        const int bph = sb_ph;
+        if (++sb_b == NB) {
+          sb_b = 0;
+          sb_ph ^= 1;
+        }
+        const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_SFULL + 8 * b, bph));
         ok = got;
         if (!got) continue;
         tc_fence_after();
@@ -547,6 +556,7 @@ __global__ void __launch_bounds__(Roles<NCH>::NTHREADS, 1)
     float *fw = reinterpret_cast<float *>(ctrl + C_F) + (warp - W_P2) * TILE;
     volatile int *go = reinterpret_cast<volatile int *>(ctrl + C_GO);
     int it = 0;
+    int vb_b = 0, vb_ph = 0;  // the tile's buffer and its use parity
     bool ok = true;
     for (int k = 0; k < njobs; ++k) {
       const int j = job_of(k);
@@ -605,9 +615,14 @@ __global__ void __launch_bounds__(Roles<NCH>::NTHREADS, 1)
       }
       named_bar(2, 32 * NP2);
       for (int i = 0; i < n; ++i, ++it) {
-        if (VS > 1 && it % VS != vset) continue;  // the other set's tile
-        const int b = it % NB;
-        const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_PDONE + 8 * b, (it / NB) & 1));
+        const int b = vb_b;
+        const int bph = vb_ph;
+        if (++vb_b == NB) {
+          vb_b = 0;
+          vb_ph ^= 1;
+        }
+        if (VS > 1 && (it & (VS - 1)) != vset) continue;  // the other set's tile
+        const bool got = __all_sync(0xffffffffu, ok && ab.wait(ctl + C_PDONE + 8 * b, bph));
         ok = got;
         const int kt = J.t0 + i;
         const int key = kt * TILE + q * 32 + lane;
