@@ -209,3 +209,38 @@ def test_lse_route_full_size_mistral_and_opt_sampled(kvc):
     for (b, h) in [(0, 0), (63, 31), (17, 5)]:
         ref = OS.window_votes(f64(Q[b, h:h + 1]), f64(K[b, h]))
         assert_votes_close(scores[0, b, h].cpu().numpy(), ref, "opt scores (%d,%d)" % (b, h))
+
+
+def test_lse_route_argument_errors_launch_nothing(kvc):
+    """The C entry points check their arguments before any launch: NULL pointers, sizes out
+    of range and misaligned bases return their codes and leave the device status clear."""
+    import ctypes
+
+    from attention_score_kv_snapkv_gb300._binding import H2OParams, SnapKVParams
+    lib = kvc.lib()
+    dev = torch.device("cuda")
+    q = torch.zeros((1, 1, 2, 64, 64), dtype=torch.bfloat16, device=dev)
+    k = torch.zeros((1, 1, 1, 64, 64), dtype=torch.bfloat16, device=dev)
+    lse = torch.zeros((1, 1, 2, 64), dtype=torch.float32, device=dev)
+    votes = torch.zeros((1, 1, 1, 64), dtype=torch.float32, device=dev)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    p = SnapKVParams(1, 1, 2, 1, 64, 64, 8, 0, 1, 1, 1, 0)
+    assert lib.snapkv_votes_from_lse(ctypes.byref(p), P(q), P(k), None, P(votes), None) == 1
+    assert lib.snapkv_votes_from_lse(ctypes.byref(p), P(q), P(k), P(lse), None, None) == 1
+    assert lib.snapkv_votes_from_lse(None, P(q), P(k), P(lse), P(votes), None) == 1
+    bad = SnapKVParams(1, 1, 2, 1, 64, 64, 65, 0, 1, 1, 1, 0)  # n_query > prompt_len
+    assert lib.snapkv_votes_from_lse(ctypes.byref(bad), P(q), P(k), P(lse), P(votes), None) == 2
+    bad = SnapKVParams(1, 1, 2, 1, 96, 64, 8, 0, 1, 1, 1, 0)  # head_dim 96
+    assert lib.snapkv_votes_from_lse(ctypes.byref(bad), P(q), P(k), P(lse), P(votes), None) == 2
+    off = ctypes.c_void_p(q.data_ptr() + 2)  # not 16-byte aligned
+    assert lib.snapkv_votes_from_lse(ctypes.byref(p), off, P(k), P(lse), P(votes), None) == 3
+    out = torch.empty_like(q)
+    assert lib.prefill_attention_lse(ctypes.byref(p), P(q), P(k), P(k), P(out), None, None) == 1
+    hp = H2OParams(1, 1, 2, 1, 64, 8, 8)
+    st = kvc.H2OState(1, 1, 1, 64, 8, 8, dev)
+    sc = st.c_struct()
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device=dev)
+    assert lib.h2o_prefill_from_votes(ctypes.byref(hp), 64, None, P(k), P(k), ctypes.byref(sc),
+                                      P(ws), ws.numel(), None) == 1
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
