@@ -31,6 +31,8 @@ constexpr int CHUNK = 4096;      // pooling staging floats (aliases the histogra
 constexpr int SMEM_KEYS_MAX = 48 * 1024;  // candidates kept in shared memory
 
 constexpr int RUN = 32;          // positions per thread in the kernel-7 pooling path
+constexpr int CHUNK_C = NT * RUN;  // candidates per CTA of the chunked path
+constexpr int RUN2 = 16;         // candidates per thread in the merge of the chunked path
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
@@ -50,6 +52,10 @@ struct TopkP {
   int32_t *sel;        // [U, cap] output positions
   int cap;
   uint32_t *kglobal;   // [U, n_cand] keys when they do not fit in shared memory
+  // chunked path (long prompts): each chunk's local top-k, positions and keys
+  int nchunks;         // chunks of CHUNK_C candidates per unit
+  int32_t *cpos;       // [U, nchunks, cap]
+  uint32_t *ckey;      // [U, nchunks, cap]
 };
 
 // shared memory (32-bit words): per-warp histograms [NWARP][NBIN] (the pooling stage
@@ -114,6 +120,173 @@ __device__ __forceinline__ void find_bin(const uint32_t *hist, int *misc, int ne
   __syncthreads();
 }
 
+// The pool-kernel-7 path with each thread's keys in registers: pooled keys of the
+// candidates [c0, c0 + nc) of a unit whose votes v hold nall candidates (the windows read
+// up to three positions beyond the range where those exist, else the padding), then the
+// positions of the k largest (equal keys: lower position first), ascending, into
+// sel_out[0..k) and, with key_out, their keys beside them.  nc <= NT * RUN, 1 <= k <= nc.
+// Shared memory: the histogram region, misc, and key_words(nc) words at `stage`.
+__device__ __forceinline__ void select_run(const float *v, int c0, int nc, int nall, int k,
+                                           bool avg, int32_t *sel_out, uint32_t *key_out,
+                                           uint32_t *sm, uint32_t *stage, int *misc) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float pad = avg ? 0.f : -INFINITY;  // value beyond both ends of the candidates
+  const float inv = 1.f / 7.f;
+  // pool kernel 7, one run of 32 consecutive positions per thread: the votes go to
+  // shared memory with one pad word per 32 (a thread's run is then conflict-free
+  // across the warp); the run and its halo are read into registers and the window
+  // maxima (or sums) formed there.  Staged index jj holds position jj - 3.
+  float *vs = reinterpret_cast<float *>(stage);
+  const float *vc = v + c0;
+  if ((reinterpret_cast<uintptr_t>(vc) & 15u) == 0) {
+    // 16-byte loads, all of a thread's in flight together
+    const int n4 = nc >> 2;
+    const float4 *v4 = reinterpret_cast<const float4 *>(vc);
+    for (int i1 = tid; i1 < n4; i1 += 8 * NT) {
+      float4 t8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int i = i1 + e * NT;
+        t8[e] = i < n4 ? __ldg(v4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int i = i1 + e * NT;
+        if (i < n4) {
+          const int jj = 4 * i + 3;
+          vs[kidx(jj)] = t8[e].x;
+          vs[kidx(jj + 1)] = t8[e].y;
+          vs[kidx(jj + 2)] = t8[e].z;
+          vs[kidx(jj + 3)] = t8[e].w;
+        }
+      }
+    }
+    if (tid < 3) {  // the halos: three positions below and above the range
+      const int lo = c0 - 3 + tid, hi = c0 + nc + tid;
+      vs[kidx(tid)] = lo >= 0 ? __ldg(v + lo) : pad;
+      vs[kidx(nc + 3 + tid)] = hi < nall ? __ldg(v + hi) : pad;
+    } else if (tid < 3 + (nc & 3)) {  // the last nc % 4 candidates
+      const int q = (nc & ~3) + tid - 3;
+      vs[kidx(q + 3)] = __ldg(vc + q);
+    }
+  } else {
+    // eight loads in flight per thread before the stores
+    for (int j1 = tid; j1 < nc + 6; j1 += 8 * NT) {
+      float t8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int q = c0 + j1 + e * NT - 3;  // the position staged at index j1 + e NT
+        t8[e] = (j1 + e * NT < nc + 6 && q >= 0 && q < nall) ? __ldg(v + q) : pad;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int j = j1 + e * NT;
+        if (j < nc + 6) vs[kidx(j)] = t8[e];
+      }
+    }
+  }
+  uint32_t *hist = sm + SM_HIST;
+  for (int b = tid; b < NB; b += NT) hist[b] = 0;
+  __syncthreads();
+  const int j0 = tid * RUN;
+  uint32_t key[RUN];  // this thread's pooled keys (positions j0 ..), 0 past the candidates
+  {
+    float w[RUN + 6];
+#pragma unroll
+    for (int i = 0; i < RUN + 6; ++i) {
+      const int jj = j0 + i;  // staged index of position j0 + i - 3
+      w[i] = jj < nc + 6 ? vs[kidx(jj)] : pad;
+    }
+#pragma unroll
+    for (int i = 0; i < RUN; ++i) {
+      const float m = avg ? (((((w[i] + w[i + 1]) + w[i + 2]) + w[i + 3]) + w[i + 4]) + w[i + 5] + w[i + 6]) * inv
+                          : fmax3(fmax3(w[i], w[i + 1], w[i + 2]), fmax3(w[i + 3], w[i + 4], w[i + 5]), w[i + 6]);
+      key[i] = j0 + i < nc ? order_key(m) : 0u;
+    }
+  }
+  // radix pass 0 (bits 31-21): neighbouring pooled values mostly share their top digit,
+  // so a thread adds each run of equal digits with one shared atomic
+  {
+    uint32_t cur = 0xffffffffu, cnt = 0;
+#pragma unroll
+    for (int i = 0; i < RUN; ++i) {
+      if (j0 + i < nc) {
+        const uint32_t b = key[i] >> 21;
+        if (b != cur) {
+          if (cnt) atomicAdd(&hist[cur], cnt);
+          cur = b;
+          cnt = 0;
+        }
+        ++cnt;
+      }
+    }
+    if (cnt) atomicAdd(&hist[cur], cnt);
+  }
+  __syncthreads();
+  find_bin<NB / NT>(hist, misc, k);
+  const uint32_t b0 = (uint32_t)misc[M_BIN];
+  int need = misc[M_NEED];
+#pragma unroll
+  for (int b = 0; b < NB / NT; ++b) hist[tid * (NB / NT) + b] = 0;  // own bins (read above)
+  __syncthreads();
+  // radix pass 1 (bits 20-10) over the keys of bucket b0
+#pragma unroll
+  for (int i = 0; i < RUN; ++i)
+    if (j0 + i < nc && (key[i] >> 21) == b0) atomicAdd(&hist[(key[i] >> 10) & (NB - 1)], 1u);
+  __syncthreads();
+  find_bin<NB / NT>(hist, misc, need);
+  const uint32_t pre = (b0 << 11) | (uint32_t)misc[M_BIN];  // key >> 10 of the bucket
+  need = misc[M_NEED];
+#pragma unroll
+  for (int b = 0; b < NB / NT; ++b) hist[tid * (NB / NT) + b] = 0;
+  __syncthreads();
+  // radix pass 2 (bits 9-0)
+#pragma unroll
+  for (int i = 0; i < RUN; ++i)
+    if (j0 + i < nc && (key[i] >> 10) == pre) atomicAdd(&hist[key[i] & 1023u], 1u);
+  __syncthreads();
+  find_bin<1024 / NT>(hist, misc, need);
+  const uint32_t T = (pre << 10) | (uint32_t)misc[M_BIN];
+  need = misc[M_NEED];
+  // compaction in position order: counts above / equal to the threshold, a block-wide
+  // exclusive scan, then each thread writes its chosen positions (ties: the first
+  // `need` equal keys by position)
+  int gt = 0, eq = 0;
+#pragma unroll
+  for (int i = 0; i < RUN; ++i) {
+    gt += (j0 + i < nc && key[i] > T) ? 1 : 0;
+    eq += (j0 + i < nc && key[i] == T) ? 1 : 0;
+  }
+  const int packed = gt | (eq << 16);
+  int incl = packed;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) misc[M_CSUM + warp] = incl;
+  __syncthreads();
+  int wbase = 0;
+  for (int w2 = 0; w2 < warp; ++w2) wbase += misc[M_CSUM + w2];
+  const int excl = wbase + incl - packed;
+  int eq_before = excl >> 16;
+  if (gt + eq > 0) {
+    int out = (excl & 0xffff) + min(eq_before, need);
+#pragma unroll
+    for (int i = 0; i < RUN; ++i) {  // branch-free: predicated stores
+      const bool valid = j0 + i < nc;
+      const bool eqT = valid && key[i] == T;
+      const bool take = (valid && key[i] > T) || (eqT && eq_before < need);
+      eq_before += eqT ? 1 : 0;
+      if (take && out < k) {
+        sel_out[out] = c0 + j0 + i;
+        if (key_out) key_out[out] = key[i];
+      }
+      out += take ? 1 : 0;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
   // Programmatic dependent launch: the gather kernel may start launching (its CTAs take
   // SM slots as these exit, and wait until this grid has completed); this grid waits for
@@ -140,154 +313,7 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
   // at once into the key array when it is in shared memory (each thread keeps its
   // pooled values in registers until every window has been read), else in chunks.
   if (in_smem && n <= RUN * NT && h == 3) {
-    // pool kernel 7, one run of 32 consecutive positions per thread: the votes go to
-    // shared memory with one pad word per 32 (a thread's run is then conflict-free
-    // across the warp); the run and its halo are read into registers and the window
-    // maxima (or sums) formed there.  Staged index jj holds position jj - 3.
-    float *vs = reinterpret_cast<float *>(kb);
-    if ((reinterpret_cast<uintptr_t>(v) & 15u) == 0) {
-      // 16-byte loads, all of a thread's in flight together
-      const int n4 = n >> 2;
-      const float4 *v4 = reinterpret_cast<const float4 *>(v);
-      for (int i1 = tid; i1 < n4; i1 += 8 * NT) {
-        float4 t8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int i = i1 + e * NT;
-          t8[e] = i < n4 ? __ldg(v4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int i = i1 + e * NT;
-          if (i < n4) {
-            const int jj = 4 * i + 3;
-            vs[kidx(jj)] = t8[e].x;
-            vs[kidx(jj + 1)] = t8[e].y;
-            vs[kidx(jj + 2)] = t8[e].z;
-            vs[kidx(jj + 3)] = t8[e].w;
-          }
-        }
-      }
-      if (tid < 3) {  // the halo
-        vs[kidx(tid)] = pad;
-        vs[kidx(n + 3 + tid)] = pad;
-      } else if (tid < 3 + (n & 3)) {  // the last n % 4 candidates
-        const int q = (n & ~3) + tid - 3;
-        vs[kidx(q + 3)] = __ldg(v + q);
-      }
-    } else {
-      // eight loads in flight per thread before the stores
-      for (int j1 = tid; j1 < n + 6; j1 += 8 * NT) {
-        float t8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int q = j1 + e * NT - 3;
-          t8[e] = (q >= 0 && q < n) ? __ldg(v + q) : pad;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = j1 + e * NT;
-          if (j < n + 6) vs[kidx(j)] = t8[e];
-        }
-      }
-    }
-    uint32_t *hist = sm + SM_HIST;
-    for (int b = tid; b < NB; b += NT) hist[b] = 0;
-    __syncthreads();
-    const int j0 = tid * RUN;
-    uint32_t key[RUN];  // this thread's pooled keys (positions j0 ..), 0 past the candidates
-    {
-      float w[RUN + 6];
-#pragma unroll
-      for (int i = 0; i < RUN + 6; ++i) {
-        const int jj = j0 + i;  // staged index of position j0 + i - 3
-        w[i] = jj < n + 6 ? vs[kidx(jj)] : pad;
-      }
-#pragma unroll
-      for (int i = 0; i < RUN; ++i) {
-        const float m = avg ? (((((w[i] + w[i + 1]) + w[i + 2]) + w[i + 3]) + w[i + 4]) + w[i + 5] + w[i + 6]) * inv
-                            : fmax3(fmax3(w[i], w[i + 1], w[i + 2]), fmax3(w[i + 3], w[i + 4], w[i + 5]), w[i + 6]);
-        key[i] = j0 + i < n ? order_key(m) : 0u;
-      }
-    }
-    // radix pass 0 (bits 31-21): neighbouring pooled values mostly share their top digit,
-    // so a thread adds each run of equal digits with one shared atomic
-    {
-      uint32_t cur = 0xffffffffu, cnt = 0;
-#pragma unroll
-      for (int i = 0; i < RUN; ++i) {
-        if (j0 + i < n) {
-          const uint32_t b = key[i] >> 21;
-          if (b != cur) {
-            if (cnt) atomicAdd(&hist[cur], cnt);
-            cur = b;
-            cnt = 0;
-          }
-          ++cnt;
-        }
-      }
-      if (cnt) atomicAdd(&hist[cur], cnt);
-    }
-    __syncthreads();
-    find_bin<NB / NT>(hist, misc, p.k);
-    const uint32_t b0 = (uint32_t)misc[M_BIN];
-    int need = misc[M_NEED];
-#pragma unroll
-    for (int b = 0; b < NB / NT; ++b) hist[tid * (NB / NT) + b] = 0;  // own bins (read above)
-    __syncthreads();
-    // radix pass 1 (bits 20-10) over the keys of bucket b0
-#pragma unroll
-    for (int i = 0; i < RUN; ++i)
-      if (j0 + i < n && (key[i] >> 21) == b0) atomicAdd(&hist[(key[i] >> 10) & (NB - 1)], 1u);
-    __syncthreads();
-    find_bin<NB / NT>(hist, misc, need);
-    const uint32_t pre = (b0 << 11) | (uint32_t)misc[M_BIN];  // key >> 10 of the bucket
-    need = misc[M_NEED];
-#pragma unroll
-    for (int b = 0; b < NB / NT; ++b) hist[tid * (NB / NT) + b] = 0;
-    __syncthreads();
-    // radix pass 2 (bits 9-0)
-#pragma unroll
-    for (int i = 0; i < RUN; ++i)
-      if (j0 + i < n && (key[i] >> 10) == pre) atomicAdd(&hist[key[i] & 1023u], 1u);
-    __syncthreads();
-    find_bin<1024 / NT>(hist, misc, need);
-    const uint32_t T = (pre << 10) | (uint32_t)misc[M_BIN];
-    need = misc[M_NEED];
-    // compaction in position order: counts above / equal to the threshold, a block-wide
-    // exclusive scan, then each thread writes its chosen positions (ties: the first
-    // `need` equal keys by position)
-    int gt = 0, eq = 0;
-#pragma unroll
-    for (int i = 0; i < RUN; ++i) {
-      gt += (j0 + i < n && key[i] > T) ? 1 : 0;
-      eq += (j0 + i < n && key[i] == T) ? 1 : 0;
-    }
-    const int packed = gt | (eq << 16);
-    int incl = packed;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    if (lane == 31) misc[M_CSUM + warp] = incl;
-    __syncthreads();
-    int wbase = 0;
-    for (int w2 = 0; w2 < warp; ++w2) wbase += misc[M_CSUM + w2];
-    const int excl = wbase + incl - packed;
-    int eq_before = excl >> 16;
-    if (gt + eq > 0) {
-      int out = (excl & 0xffff) + min(eq_before, need);
-      int32_t *sel = p.sel + (size_t)u * p.cap;
-#pragma unroll
-      for (int i = 0; i < RUN; ++i) {
-        const bool take = j0 + i < n && (key[i] > T || (key[i] == T && eq_before++ < need));
-        if (take) {
-          if (out < p.k) sel[out] = j0 + i;
-          ++out;
-        }
-      }
-    }
+    select_run(v, 0, n, n, p.k, avg, p.sel + (size_t)u * p.cap, nullptr, sm, kb, misc);
     return;
   }
   if (2 * h < CHUNK / 2) {
@@ -480,6 +506,129 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
   }
 }
 
+// Chunked path for long prompts (pool kernel 7): the global top-k (equal keys: lower
+// position first) lies inside the union of each chunk's local top-k taken with the same
+// rule, since restricted to one chunk it is a prefix of that chunk's order.  Kernel 1:
+// one CTA per (chunk of CHUNK_C candidates, unit) pools its range (the windows read the
+// neighbouring chunks' votes) and writes its local top-k, ascending, with their keys.
+// Kernel 2: one CTA per unit selects the top k of those candidates, which are in position
+// order chunk after chunk, and writes their positions ascending.
+__global__ void __launch_bounds__(NT, 2) pool_topk_chunk_kernel(const TopkP p) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  extern __shared__ uint32_t sm[];
+  int *misc = reinterpret_cast<int *>(sm + SM_MISC);
+  const int c = blockIdx.x, u = blockIdx.y;
+  const int c0 = c * CHUNK_C;
+  const int nc = min(CHUNK_C, p.n_cand - c0);
+  const size_t o = ((size_t)u * p.nchunks + c) * p.cap;
+  select_run(p.votes + (size_t)u * p.L, c0, nc, p.n_cand, min(p.k, nc), p.avg != 0, p.cpos + o,
+             p.ckey + o, sm, sm + SM_KEYS, misc);
+}
+
+__global__ void __launch_bounds__(NT, 2) topk_merge_kernel(const TopkP p) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  extern __shared__ uint32_t sm[];
+  int *misc = reinterpret_cast<int *>(sm + SM_MISC);
+  uint32_t *hist = sm + SM_HIST;
+  const int u = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // candidates: chunk c holds min(k, its length) of them; all chunks but the last hold k
+  const int last_nc = p.n_cand - (p.nchunks - 1) * CHUNK_C;
+  const int total = (p.nchunks - 1) * p.k + min(p.k, last_nc);
+  const int e0 = tid * RUN2;
+  uint32_t key[RUN2];
+  int pos[RUN2];
+#pragma unroll
+  for (int i = 0; i < RUN2; ++i) {
+    const int e = e0 + i;
+    key[i] = 0u;
+    pos[i] = -1;
+    if (e < total) {
+      const int c = e / p.k, ii = e - c * p.k;
+      const size_t o = ((size_t)u * p.nchunks + c) * p.cap + ii;
+      key[i] = p.ckey[o];
+      pos[i] = p.cpos[o];
+    }
+  }
+  for (int b = tid; b < NB; b += NT) hist[b] = 0;
+  __syncthreads();
+  // three radix digits (bits 31-21, 20-10, 9-0) over one shared histogram, as select_run
+  {
+    uint32_t cur = 0xffffffffu, cnt = 0;
+#pragma unroll
+    for (int i = 0; i < RUN2; ++i) {
+      if (e0 + i < total) {
+        const uint32_t b = key[i] >> 21;
+        if (b != cur) {
+          if (cnt) atomicAdd(&hist[cur], cnt);
+          cur = b;
+          cnt = 0;
+        }
+        ++cnt;
+      }
+    }
+    if (cnt) atomicAdd(&hist[cur], cnt);
+  }
+  __syncthreads();
+  find_bin<NB / NT>(hist, misc, p.k);
+  const uint32_t b0 = (uint32_t)misc[M_BIN];
+  int need = misc[M_NEED];
+#pragma unroll
+  for (int b = 0; b < NB / NT; ++b) hist[tid * (NB / NT) + b] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < RUN2; ++i)
+    if (e0 + i < total && (key[i] >> 21) == b0) atomicAdd(&hist[(key[i] >> 10) & (NB - 1)], 1u);
+  __syncthreads();
+  find_bin<NB / NT>(hist, misc, need);
+  const uint32_t pre = (b0 << 11) | (uint32_t)misc[M_BIN];
+  need = misc[M_NEED];
+#pragma unroll
+  for (int b = 0; b < NB / NT; ++b) hist[tid * (NB / NT) + b] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < RUN2; ++i)
+    if (e0 + i < total && (key[i] >> 10) == pre) atomicAdd(&hist[key[i] & 1023u], 1u);
+  __syncthreads();
+  find_bin<1024 / NT>(hist, misc, need);
+  const uint32_t T = (pre << 10) | (uint32_t)misc[M_BIN];
+  need = misc[M_NEED];
+  // compaction in candidate (= position) order, ties: the first `need` equal keys
+  int gt = 0, eq = 0;
+#pragma unroll
+  for (int i = 0; i < RUN2; ++i) {
+    gt += (e0 + i < total && key[i] > T) ? 1 : 0;
+    eq += (e0 + i < total && key[i] == T) ? 1 : 0;
+  }
+  const int packed = gt | (eq << 16);
+  int incl = packed;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) misc[M_CSUM + warp] = incl;
+  __syncthreads();
+  int wbase = 0;
+  for (int w2 = 0; w2 < warp; ++w2) wbase += misc[M_CSUM + w2];
+  const int excl = wbase + incl - packed;
+  int eq_before = excl >> 16;
+  if (gt + eq > 0) {
+    int out = (excl & 0xffff) + min(eq_before, need);
+    int32_t *sel = p.sel + (size_t)u * p.cap;
+#pragma unroll
+    for (int i = 0; i < RUN2; ++i) {  // branch-free: predicated stores
+      const bool valid = e0 + i < total;
+      const bool eqT = valid && key[i] == T;
+      const bool take = (valid && key[i] > T) || (eqT && eq_before < need);
+      eq_before += eqT ? 1 : 0;
+      if (take && out < p.k) sel[out] = pos[i];
+      out += take ? 1 : 0;
+    }
+  }
+}
+
 struct GatherP {
   const int32_t *sel;      // [U, cap] chosen prefix positions (first k)
   const float *votes;      // [U, L] or null
@@ -534,13 +683,22 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherP p) {
 }
 
 bool g_topk_attr[64];
+bool g_chunk_attr[64];
 
 }  // namespace
 
+// The chunked path's candidates after the selected positions and the keys.
+static size_t chunk_ws_offset(int units, int n, int cap) {
+  size_t b = (size_t)units * cap * sizeof(int32_t);
+  if (n > SMEM_KEYS_MAX) b += (size_t)units * key_words(n) * sizeof(uint32_t);
+  return (b + 255) & ~(size_t)255;
+}
+
 size_t select_ws_bytes(int units, int L, int keep_window, int cap) {
-  const size_t n = (size_t)(L > keep_window ? L - keep_window : 0);
-  size_t b = (size_t)units * cap * sizeof(int32_t);               // selected positions
-  if (n > (size_t)SMEM_KEYS_MAX) b += (size_t)units * key_words((int)n) * sizeof(uint32_t);  // keys
+  const int n = L > keep_window ? L - keep_window : 0;
+  size_t b = chunk_ws_offset(units, n, cap);  // selected positions (and keys)
+  if (n > CHUNK_C)                            // the chunked path's candidates
+    b += (size_t)units * ((n + CHUNK_C - 1) / CHUNK_C) * cap * (sizeof(int32_t) + sizeof(uint32_t));
   return (b + 255) & ~(size_t)255;
 }
 
@@ -569,18 +727,43 @@ cudaError_t launch_select_gather(const Ctx &c, const SelectArgs &a) {
     tp.sel = a.sel_ws;
     tp.cap = a.cap;
     tp.kglobal = reinterpret_cast<uint32_t *>(a.sel_ws + (size_t)a.units * a.cap);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.units);
-    cfg.blockDim = dim3(NT);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = c.stream;
+    tp.nchunks = (n_cand + CHUNK_C - 1) / CHUNK_C;
+    uint8_t *cbase = reinterpret_cast<uint8_t *>(a.sel_ws) + chunk_ws_offset(a.units, n_cand, a.cap);
+    tp.cpos = reinterpret_cast<int32_t *>(cbase);
+    tp.ckey = reinterpret_cast<uint32_t *>(cbase + (size_t)a.units * tp.nchunks * a.cap * sizeof(int32_t));
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(NT);
+    cfg.stream = c.stream;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, pool_topk_kernel, tp);
-    if (e != cudaSuccess) return e;
+    // long prompts with pool kernel 7: the chunked path when the chunks' candidates fit
+    // the merge's registers
+    const bool chunked = tp.half == 3 && n_cand > CHUNK_C && tp.nchunks * k_pick <= NT * RUN2;
+    if (chunked) {
+      if (dev < 64 && !g_chunk_attr[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(pool_topk_chunk_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (SM_KEYS + key_words(CHUNK_C)) * 4);
+        if (e != cudaSuccess) return e;
+        g_chunk_attr[dev] = true;
+      }
+      cfg.gridDim = dim3((unsigned)tp.nchunks, (unsigned)a.units);
+      cfg.dynamicSmemBytes = (size_t)(SM_KEYS + key_words(CHUNK_C)) * 4;
+      cudaError_t e = cudaLaunchKernelEx(&cfg, pool_topk_chunk_kernel, tp);
+      if (e != cudaSuccess) return e;
+      cfg.gridDim = dim3((unsigned)a.units);
+      cfg.dynamicSmemBytes = (size_t)SM_KEYS * 4;
+      e = cudaLaunchKernelEx(&cfg, topk_merge_kernel, tp);
+      if (e != cudaSuccess) return e;
+    } else {
+      cfg.gridDim = dim3((unsigned)a.units);
+      cfg.dynamicSmemBytes = (size_t)smem;
+      cudaError_t e = cudaLaunchKernelEx(&cfg, pool_topk_kernel, tp);
+      if (e != cudaSuccess) return e;
+    }
   }
   GatherP gp;
   gp.sel = a.sel_ws;

@@ -16,6 +16,7 @@ oracle as CPU baseline.  --impl reference times the oracle itself.
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -423,8 +424,29 @@ def measure_long(kvc, WL, dev, hbm_peak):
     d_ms = timed(graph.replay)
     d_bytes = sum(Ly * Bb * (4 * H * (Kb + s + 1) * Dd + 4 * w.q_heads * Dd + 4 * H * Dd)
                   for s in range(S)) / S
+    # The same compression from the window rows' log-sum-exp, which a prefill through
+    # prefill_attention_lse would return; here the harness forms it (fp32, one layer at a
+    # time) because a prefill of this prompt takes seconds.  Timed: the vote pass and the
+    # selection only.
+    lse = torch.full((Ly, Bb, w.q_heads, Ll), float("nan"), dtype=torch.float32, device=dev)
+    G = w.q_heads // H
+    rows = torch.arange(Ll - Wn, Ll, device=dev)
+    keys = torch.arange(Ll, device=dev)
+    for l in range(Ly):
+        for b in range(Bb):
+            qf = x["Q_win"][l, b].float().view(H, G * Wn, Dd)
+            sc = torch.matmul(qf, x["K"][l, b].float().transpose(1, 2)) / math.sqrt(Dd)
+            sc = sc.view(H, G, Wn, Ll).masked_fill(keys.view(1, 1, 1, Ll) > rows.view(1, 1, Wn, 1),
+                                                    float("-inf"))
+            lse[l, b, :, Ll - Wn:] = torch.logsumexp(sc, dim=-1).view(w.q_heads, Wn)
+            del qf, sc
+    votes = torch.empty((Ly, Bb, H, Ll), dtype=torch.float32, device=dev)
+    v_ms = _events_ms(lambda: kvc.snapkv_votes_from_lse(x["Q_win"], x["K"], lse, votes_out=votes), 5, 3)
+    s_ms = _events_ms(lambda: kvc.snapkv_select(votes, x["K"], x["V"], keep_window=Wn,
+                                                pool_kernel=w.pool_kernel, budget=Kb, cap=cap), 5, 3)
+    v_bytes = Ly * Bb * (H * Ll * Dd * 2 + w.q_heads * Wn * Dd * 2 + w.q_heads * Wn * 4 + H * Ll * 4)
     status = kvc.kvc_device_status()
-    del x, kc, vc, graph
+    del x, kc, vc, graph, lse, votes
     torch.cuda.empty_cache()
     return {"workload": w.name, "compress_ms": c_ms, "prefix_tokens_per_s": Bb * Ll / (c_ms / 1e3),
             "compress_GBps": c_bytes / (c_ms / 1e3) / 1e9,
@@ -432,7 +454,12 @@ def measure_long(kvc, WL, dev, hbm_peak):
             "decode_ms_per_step": d_ms, "decode_GBps": d_bytes / (d_ms / 1e3) / 1e9,
             "decode_frac_of_hbm_peak": d_bytes / (d_ms / 1e3) / 1e9 / hbm_peak,
             "decode_launch": "one call per step for all layers; the 128 calls replayed as a CUDA graph",
-            "decode_eager_ms_per_step": d_eager, "device_status": status}
+            "decode_eager_ms_per_step": d_eager,
+            "votes_from_lse_ms": v_ms, "votes_from_lse_GBps": v_bytes / (v_ms / 1e3) / 1e9,
+            "votes_from_lse_frac_of_hbm_peak": v_bytes / (v_ms / 1e3) / 1e9 / hbm_peak,
+            "compress_from_lse_ms": v_ms + s_ms,
+            "compress_from_lse_prefix_tokens_per_s": Bb * Ll / ((v_ms + s_ms) / 1e3),
+            "device_status": status}
 
 
 def measure_h2o(kvc, WL, dev, hbm_peak, steps=64, n_heavy=None, n_recent=None):

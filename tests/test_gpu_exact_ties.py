@@ -6,10 +6,12 @@
   here are multiples of 1/4 below 3, so every pooled value (a maximum, or a window sum
   of such multiples, which fp32 forms exactly) is exact in fp32 and in fp64: the
   oracle's fp64 selection is then the only correct answer, and the GPU's must equal it.
-  Each case runs one of the selection kernel's radix paths: pool 7 with the candidates
-  in registers, keys in shared memory (other pool sizes, or more than 16384
-  candidates), and keys in global memory (more than 49152 candidates); unaligned vote
-  rows take the scalar staging path.
+  Each case runs one of the selection kernels' radix paths: pool 7 with the candidates
+  in registers; pool 7 over more than 16384 candidates in chunks of 16384 (each chunk's
+  local top-k, then their merge; the plateaus straddle the chunk boundaries); keys in
+  shared memory (other pool sizes, or chunks whose candidates exceed the merge's 8192);
+  keys in global memory (more than 49152 candidates); unaligned vote rows take the
+  scalar staging path.
 * H2O eviction (H2O article, 処理の流れ): among exactly equal smallest cumulative
   scores the entry with the higher position is evicted (the lower position is kept).
   The planted state has several evictable entries with the same score whose keys are
@@ -35,7 +37,11 @@ SELECT_CASES = [
     ("registers-avg7", 4096, 32, 7, 480, True),
     ("shared-max5", 3000, 16, 5, 300, False),
     ("shared-max1", 5000, 8, 1, 700, False),
-    ("shared-max7-20000", 20000, 32, 7, 3000, False),
+    ("shared-max7-20000", 20000, 32, 7, 5000, False),
+    ("chunked-max7-20000", 20000, 32, 7, 3000, False),
+    ("chunked-avg7-40000", 40000, 32, 7, 992, True),
+    ("chunked-max7-short-last-chunk", 16884, 32, 7, 4000, False),
+    ("chunked-unaligned-avg7-33001", 33001, 32, 7, 1500, True),
     ("shared-avg5", 3000, 16, 5, 300, True),
     ("global-max7-60000", 60000, 32, 7, 9000, False),
     ("global-avg3-60000", 60000, 32, 3, 992, True),

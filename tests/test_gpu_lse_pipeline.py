@@ -244,3 +244,26 @@ def test_lse_route_argument_errors_launch_nothing(kvc):
                                       P(ws), ws.numel(), None) == 1
     torch.cuda.synchronize()
     assert kvc.kvc_device_status() == 0
+
+
+def test_votes_from_lse_long_context_sampled(kvc):
+    """One layer of the long-context prompt (32 MHA heads, L = 131072, window 32): the
+    window rows' log-sum-exp from the oracle (fp64, every head), then the vote kernel
+    against the oracle's window votes for sampled heads."""
+    dev = torch.device("cuda")
+    w = W.LONG
+    x = W.snapkv_prompt(w, W.seed_of(3, 5), dev, layers=1)
+    Qw, K = x["Q_win"], x["K"]
+    L, Wn, H, D = w.prompt_len, w.window, w.kv_heads, w.head_dim
+    lse = np.full((1, 1, w.q_heads, L), np.nan)
+    for h in range(H):
+        qh, kh = f64(Qw[0, 0, h]), f64(K[0, 0, h])
+        logits = qh @ kh.T / np.sqrt(D)                      # [Wn, L]
+        for r in range(Wn):
+            lse[0, 0, h, L - Wn + r] = OA.log_sum_exp(logits[r, :L - Wn + r + 1])
+    votes = kvc.snapkv_votes_from_lse(Qw, K, torch.as_tensor(lse, dtype=torch.float32).to(dev))
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    for h in (0, 17, H - 1):
+        ref = OS.window_votes(f64(Qw[0, 0, h:h + 1]), f64(K[0, 0, h]))
+        assert_votes_close(votes[0, 0, h].cpu().numpy(), ref, "long-context votes (head %d)" % h)
