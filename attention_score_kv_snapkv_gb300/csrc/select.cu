@@ -251,12 +251,22 @@ __device__ __forceinline__ void select_run(const float *v, int c0, int nc, int n
   // compaction in position order: counts above / equal to the threshold, a block-wide
   // exclusive scan, then each thread writes its chosen positions (ties: the first
   // `need` equal keys by position)
-  int gt = 0, eq = 0;
+  // this thread's keys above and equal to the threshold, as bit masks over its run
+  uint32_t gtm = 0u, eqm = 0u;
 #pragma unroll
   for (int i = 0; i < RUN; ++i) {
-    gt += (j0 + i < nc && key[i] > T) ? 1 : 0;
-    eq += (j0 + i < nc && key[i] == T) ? 1 : 0;
+    const bool valid = j0 + i < nc;
+    gtm |= (valid && key[i] > T) ? (1u << i) : 0u;
+    eqm |= (valid && key[i] == T) ? (1u << i) : 0u;
   }
+  // keys for key_out are read back by position below: staged where the votes were (every
+  // thread has finished reading the votes: barriers have passed since)
+  if (key_out) {
+#pragma unroll
+    for (int i = 0; i < RUN; ++i)
+      if (j0 + i < nc) stage[kidx(j0 + i)] = key[i];
+  }
+  const int gt = __popc(gtm), eq = __popc(eqm);
   const int packed = gt | (eq << 16);
   int incl = packed;
 #pragma unroll
@@ -269,21 +279,24 @@ __device__ __forceinline__ void select_run(const float *v, int c0, int nc, int n
   int wbase = 0;
   for (int w2 = 0; w2 < warp; ++w2) wbase += misc[M_CSUM + w2];
   const int excl = wbase + incl - packed;
-  int eq_before = excl >> 16;
-  if (gt + eq > 0) {
-    int out = (excl & 0xffff) + min(eq_before, need);
-#pragma unroll
-    for (int i = 0; i < RUN; ++i) {  // branch-free: predicated stores
-      const bool valid = j0 + i < nc;
-      const bool eqT = valid && key[i] == T;
-      const bool take = (valid && key[i] > T) || (eqT && eq_before < need);
-      eq_before += eqT ? 1 : 0;
-      if (take && out < k) {
-        sel_out[out] = c0 + j0 + i;
-        if (key_out) key_out[out] = key[i];
-      }
-      out += take ? 1 : 0;
+  const int eq_before = excl >> 16;
+  // the taken keys: every key above the threshold, and of the equal ones the first
+  // `need` by position across the CTA, i.e. this thread's first need - eq_before
+  uint32_t m = gtm;
+  for (int t = max(0, min(eq, need - eq_before)); t > 0; --t) {
+    const uint32_t low = eqm & (0u - eqm);
+    m |= low;
+    eqm ^= low;
+  }
+  int out = (excl & 0xffff) + min(eq_before, need);
+  while (m) {  // ascending positions: lowest bit first
+    const int i = __ffs(m) - 1;
+    m &= m - 1;
+    if (out < k) {
+      sel_out[out] = c0 + j0 + i;
+      if (key_out) key_out[out] = stage[kidx(j0 + i)];
     }
+    ++out;
   }
 }
 
