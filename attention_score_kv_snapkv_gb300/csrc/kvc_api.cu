@@ -104,7 +104,7 @@ kvc_status plan_snapkv(const kvc_snapkv_params *p, bool want_scores, int num_sms
   if ((long long)s->G * p->n_query > kMaxRows) return KVC_ERR_SHAPE;
   s->R = s->G * p->n_query;
   if (s->units * p->prompt_len > kMaxRows || s->units * s->R > kMaxRows ||
-      s->units * p->cap > kMaxRows)
+      s->units * p->cap > kMaxRows || p->cap > 65535 * 32)  // the gather's grid: cap / 32 <= 65535
     return KVC_ERR_SHAPE;
   s->identity = p->budget >= p->prompt_len || p->keep_window >= p->prompt_len;
   if (!s->identity && p->budget < p->keep_window) return KVC_ERR_BUDGET;

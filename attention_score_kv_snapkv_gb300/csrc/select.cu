@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_chunk_kernel(const TopkP p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ uint32_t sm[];
   int *misc = reinterpret_cast<int *>(sm + SM_MISC);
-  const int c = blockIdx.x, u = blockIdx.y;
+  const int u = blockIdx.x, c = blockIdx.y;  // units on x: more than 65535 of them fit
   const int c0 = c * CHUNK_C;
   const int nc = min(CHUNK_C, p.n_cand - c0);
   const size_t o = ((size_t)u * p.nchunks + c) * p.cap;
@@ -654,12 +654,12 @@ struct GatherP {
   uint32_t *status;
 };
 
-// grid (ceil(cap / 32), U); 256 threads; each CTA fills 32 rows of one unit.
+// grid (U, ceil(cap / 32)); 256 threads; each CTA fills 32 rows of one unit.
 __global__ void __launch_bounds__(256) gather_kernel(const GatherP p) {
   // programmatic dependent launch: wait for the kernel that wrote the positions / votes
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int u = blockIdx.y;
-  const int r0 = blockIdx.x * 32;
+  const int u = blockIdx.x;  // units on x: more than 65535 of them fit
+  const int r0 = blockIdx.y * 32;
   __shared__ int spos[32];
   if (threadIdx.x < 32) {
     const int s = r0 + threadIdx.x;
@@ -678,7 +678,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherP p) {
       p.pos_out[(size_t)u * p.cap + s] = pos;
       if (p.kept) p.kept[(size_t)u * p.cap + s] = pos >= 0 ? p.votes[(size_t)u * p.L + pos] : 0.f;
     }
-    if (blockIdx.x == 0 && threadIdx.x == 0) p.n_valid_out[u] = p.n_keep;
+    if (blockIdx.y == 0 && threadIdx.x == 0) p.n_valid_out[u] = p.n_keep;
   }
   __syncthreads();
   const int rv = p.row_vecs;
@@ -763,7 +763,7 @@ cudaError_t launch_select_gather(const Ctx &c, const SelectArgs &a) {
         if (e != cudaSuccess) return e;
         g_chunk_attr[dev] = true;
       }
-      cfg.gridDim = dim3((unsigned)tp.nchunks, (unsigned)a.units);
+      cfg.gridDim = dim3((unsigned)a.units, (unsigned)tp.nchunks);
       cfg.dynamicSmemBytes = (size_t)(SM_KEYS + key_words(CHUNK_C)) * 4;
       cudaError_t e = cudaLaunchKernelEx(&cfg, pool_topk_chunk_kernel, tp);
       if (e != cudaSuccess) return e;
@@ -797,7 +797,7 @@ cudaError_t launch_select_gather(const Ctx &c, const SelectArgs &a) {
   gp.row_vecs = a.D / 8;
   gp.status = c.status;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((a.cap + 31) / 32), (unsigned)a.units);
+  cfg.gridDim = dim3((unsigned)a.units, (unsigned)((a.cap + 31) / 32));
   cfg.blockDim = dim3(256);
   cfg.stream = c.stream;
   cudaLaunchAttribute at[1];

@@ -109,7 +109,8 @@ typedef struct {
   int32_t keep_window; /* W_keep >= 0: trailing prompt positions always kept (SnapKV: W) */
   int32_t pool_kernel; /* odd P >= 1: 1D pooling kernel over the vote (1 = no pooling) */
   int32_t budget;      /* Kb: kept entries including the window; W_keep <= Kb */
-  int32_t cap;         /* rows per unit of the output cache; cap >= min(Kb, L) */
+  int32_t cap;         /* rows per unit of the output cache; cap >= min(Kb, L),
+                          cap <= 2097120 (65535 * 32) */
   int32_t pool_avg;    /* 0: max-pool (the SnapKV default); 1: average pool, the window's sum
                           divided by P with zeros beyond both ends of the candidates */
 } kvc_snapkv_params;

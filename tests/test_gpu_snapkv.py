@@ -239,3 +239,29 @@ def test_value_rows_from_pinned_host_memory(kvc, case):
     # pageable host memory is refused before anything is launched
     with pytest.raises(Exception):
         kvc.snapkv_compress(Q, K, x["V"], **kw)
+
+
+def test_more_units_than_a_grid_dimension_holds(kvc):
+    """70000 units (beyond the 65535 a grid's y or z dimension takes): every unit is
+    compressed; sampled units against the oracle, and the last unit's rows gathered."""
+    Ly, B, Hq, Hkv, D, L, Wn, P, Kb = 1, 70000, 1, 1, 64, 64, 8, 3, 16
+    g = torch.Generator().manual_seed(70000)
+    dev = torch.device("cuda")
+    Q = torch.randn((Ly, B, Hq, Wn, D), generator=g).to(torch.bfloat16).to(dev)
+    K = torch.randn((Ly, B, Hkv, L, D), generator=g).to(torch.bfloat16).to(dev)
+    V = torch.randn((Ly, B, Hkv, L, D), generator=g).to(torch.bfloat16).to(dev)
+    res = kvc.snapkv_compress(Q, K, V, keep_window=Wn, pool_kernel=P, budget=Kb, want_votes=True)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    assert (res["n_valid"] == Kb).all()
+    for b in (0, 12345, 65535, 65536, B - 1):
+        votes_ref = OS.window_votes(f64(Q[0, b]), f64(K[0, b, 0]))
+        assert_votes_close(res["votes"][0, b, 0].cpu().numpy(), votes_ref, "votes unit %d" % b)
+        pooled = OS.max_pool_1d(votes_ref[:L - Wn], P)
+        got = res["pos"][0, b, 0].cpu().numpy()
+        assert list(got[Kb - Wn:]) == list(range(L - Wn, L))
+        check_selected_set(got[:Kb - Wn], OS.top_k_lowest_index(pooled, Kb - Wn), pooled, Kb - Wn,
+                           "unit %d" % b)
+        idx = torch.as_tensor(got, dtype=torch.long, device=dev)
+        assert torch.equal(res["k"][0, b, 0], K[0, b, 0, idx])
+        assert torch.equal(res["v"][0, b, 0], V[0, b, 0, idx])
