@@ -695,7 +695,70 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherP p) {
   }
 }
 
+// The short-prompt path (pool kernel 7, candidates in registers) with the gather fused in:
+// one CTA per unit selects its positions into shared memory (where the votes were staged)
+// and then copies the unit's kept K/V rows itself, so the copies of early units overlap
+// the selection of later ones instead of waiting for a separate gather launch.
+__global__ void __launch_bounds__(NT, 2) pool_topk_gather_kernel(const TopkP p, const GatherP gp) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  extern __shared__ uint32_t sm[];
+  int *misc = reinterpret_cast<int *>(sm + SM_MISC);
+  uint32_t *kb = sm + SM_KEYS;
+  int32_t *spos = reinterpret_cast<int32_t *>(kb);  // the chosen positions [k]
+  const int u = blockIdx.x, tid = threadIdx.x;
+  select_run(p.votes + (size_t)u * p.L, 0, p.n_cand, p.n_cand, p.k, p.avg != 0, spos, nullptr, sm,
+             kb, misc);
+  __syncthreads();
+  // positions of every cache row (-1 past n_keep), the kept scores, n_valid
+  for (int r = tid; r < gp.cap; r += NT) {
+    int pos = -1;
+    if (r < gp.n_keep) {
+      pos = r < gp.k_pick ? spos[r] : gp.L - gp.keep_window + (r - gp.k_pick);
+      if (pos < 0 || pos >= gp.L) {  // never expected: keep every access in bounds
+        set_status(gp.status, KVC_DEV_BAD_STATE);
+        pos = -1;
+      }
+    }
+    gp.pos_out[(size_t)u * gp.cap + r] = pos;
+    if (gp.kept) gp.kept[(size_t)u * gp.cap + r] = pos >= 0 ? gp.votes[(size_t)u * gp.L + pos] : 0.f;
+  }
+  if (tid == 0) gp.n_valid_out[u] = gp.n_keep;
+  // the kept rows: 16-byte pieces, eight loads in flight per thread
+  const int rv = gp.row_vecs, rvs = rv == 16 ? 4 : 3;  // D / 8 = 16 or 8 pieces a row
+  const int total = gp.n_keep * rv;
+  for (int e0 = tid; e0 < total; e0 += 4 * NT) {
+    uint4 kk[4], vv[4];
+    size_t dst[4];
+    bool ok[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + j * NT;
+      ok[j] = e < total;
+      dst[j] = 0;
+      if (ok[j]) {
+        const int r = e >> rvs, c = e & (rv - 1);
+        const int pos = r < gp.k_pick ? spos[r] : gp.L - gp.keep_window + (r - gp.k_pick);
+        ok[j] = pos >= 0 && pos < gp.L;
+        if (ok[j]) {
+          const size_t src = ((size_t)u * gp.L + pos) * rv + c;
+          kk[j] = __ldg(gp.k + src);
+          vv[j] = __ldg(gp.v + src);
+          dst[j] = ((size_t)u * gp.cap + r) * rv + c;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (ok[j]) {
+        gp.ko[dst[j]] = kk[j];
+        gp.vo[dst[j]] = vv[j];
+      }
+  }
+}
+
 bool g_topk_attr[64];
+bool g_fused_attr[64];
 bool g_chunk_attr[64];
 
 }  // namespace
@@ -719,6 +782,24 @@ cudaError_t launch_select_gather(const Ctx &c, const SelectArgs &a) {
   const int n_cand = a.L - a.keep_window;
   const int n_keep = a.identity ? a.L : a.budget;
   const int k_pick = a.identity ? 0 : a.budget - a.keep_window;
+  GatherP gp;
+  gp.sel = a.sel_ws;
+  gp.votes = a.votes;
+  gp.k = reinterpret_cast<const uint4 *>(a.k);
+  gp.v = reinterpret_cast<const uint4 *>(a.v);
+  gp.ko = reinterpret_cast<uint4 *>(a.k_out);
+  gp.vo = reinterpret_cast<uint4 *>(a.v_out);
+  gp.pos_out = a.pos_out;
+  gp.n_valid_out = a.n_valid_out;
+  gp.kept = a.kept_scores;
+  gp.L = a.L;
+  gp.cap = a.cap;
+  gp.k_pick = k_pick;
+  gp.n_keep = n_keep;
+  gp.keep_window = a.keep_window;
+  gp.identity = a.identity;
+  gp.row_vecs = a.D / 8;
+  gp.status = c.status;
   if (!a.identity && k_pick > 0) {
     int dev = 0;
     cudaGetDevice(&dev);
@@ -755,6 +836,20 @@ cudaError_t launch_select_gather(const Ctx &c, const SelectArgs &a) {
     // long prompts with pool kernel 7: the chunked path when the chunks' candidates fit
     // the merge's registers
     const bool chunked = tp.half == 3 && n_cand > CHUNK_C && tp.nchunks * k_pick <= NT * RUN2;
+    // short prompts with pool kernel 7: selection and gather in one kernel
+    const bool fused = tp.half == 3 && n_cand <= CHUNK_C && (a.D == 64 || a.D == 128);
+    if (fused) {
+      if (dev < 64 && !g_fused_attr[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(pool_topk_gather_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (SM_KEYS + key_words(CHUNK_C)) * 4);
+        if (e != cudaSuccess) return e;
+        g_fused_attr[dev] = true;
+      }
+      cfg.gridDim = dim3((unsigned)a.units);
+      cfg.dynamicSmemBytes = (size_t)smem;
+      return cudaLaunchKernelEx(&cfg, pool_topk_gather_kernel, tp, gp);
+    }
     if (chunked) {
       if (dev < 64 && !g_chunk_attr[dev]) {
         cudaError_t e = cudaFuncSetAttribute(pool_topk_chunk_kernel,
@@ -778,24 +873,6 @@ cudaError_t launch_select_gather(const Ctx &c, const SelectArgs &a) {
       if (e != cudaSuccess) return e;
     }
   }
-  GatherP gp;
-  gp.sel = a.sel_ws;
-  gp.votes = a.votes;
-  gp.k = reinterpret_cast<const uint4 *>(a.k);
-  gp.v = reinterpret_cast<const uint4 *>(a.v);
-  gp.ko = reinterpret_cast<uint4 *>(a.k_out);
-  gp.vo = reinterpret_cast<uint4 *>(a.v_out);
-  gp.pos_out = a.pos_out;
-  gp.n_valid_out = a.n_valid_out;
-  gp.kept = a.kept_scores;
-  gp.L = a.L;
-  gp.cap = a.cap;
-  gp.k_pick = k_pick;
-  gp.n_keep = n_keep;
-  gp.keep_window = a.keep_window;
-  gp.identity = a.identity;
-  gp.row_vecs = a.D / 8;
-  gp.status = c.status;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.units, (unsigned)((a.cap + 31) / 32));
   cfg.blockDim = dim3(256);
