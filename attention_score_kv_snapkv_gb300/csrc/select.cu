@@ -15,10 +15,13 @@
 //            ascending positions (per-thread runs, one block-wide scan).
 //   Pool kernel 7 with at most 32 candidates per thread (the usual SnapKV setting) keeps
 //   each thread's 32 keys in registers and selects with three digits (11, 11, 10 bits)
-//   over one shared histogram; other pool sizes and longer prompts keep the keys in
-//   shared (else global) memory and select with four 8-bit digits over per-warp
-//   histograms.
-// gather_kernel: 16-byte vectorised copy of the kept K/V rows, positions, scores.
+//   over one shared histogram -- in pool_topk_gather_kernel, which then gathers the
+//   unit's rows itself; longer prompts with pool kernel 7 go in chunks of that size
+//   (pool_topk_chunk_kernel, then topk_merge_kernel, which gathers); other pool sizes
+//   keep the keys in shared (else global) memory and select with four 8-bit digits over
+//   per-warp histograms.
+// gather_kernel: 16-byte vectorised copy of the kept K/V rows, positions, scores (after
+//   pool_topk_kernel, or alone when every position is kept).
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -325,10 +328,7 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
   // votes are staged through shared memory (coalesced, read once from L2): all of them
   // at once into the key array when it is in shared memory (each thread keeps its
   // pooled values in registers until every window has been read), else in chunks.
-  if (in_smem && n <= RUN * NT && h == 3) {
-    select_run(v, 0, n, n, p.k, avg, p.sel + (size_t)u * p.cap, nullptr, sm, kb, misc);
-    return;
-  }
+  // (pool kernel 7 over at most NT * RUN candidates runs in pool_topk_gather_kernel)
   if (2 * h < CHUNK / 2) {
     float *stage = reinterpret_cast<float *>(sm + SM_HIST);
     const int step = CHUNK - 2 * h;
@@ -519,13 +519,118 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_kernel(const TopkP p) {
   }
 }
 
+struct GatherP {
+  const int32_t *sel;      // [U, cap] chosen prefix positions (first k)
+  const float *votes;      // [U, L] or null
+  const uint4 *k, *v;      // [U, L, D]
+  uint4 *ko, *vo;          // [U, cap, D]
+  int32_t *pos_out;        // [U, cap]
+  int32_t *n_valid_out;    // [U]
+  float *kept;             // [U, cap] or null
+  int L, cap, k_pick, n_keep, keep_window, identity, row_vecs;  // row_vecs = D / 8
+  uint32_t *status;
+};
+
+// grid (U, ceil(cap / 32)); 256 threads; each CTA fills 32 rows of one unit.
+__global__ void __launch_bounds__(256) gather_kernel(const GatherP p) {
+  // programmatic dependent launch: wait for the kernel that wrote the positions / votes
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int u = blockIdx.x;  // units on x: more than 65535 of them fit
+  const int r0 = blockIdx.y * 32;
+  __shared__ int spos[32];
+  if (threadIdx.x < 32) {
+    const int s = r0 + threadIdx.x;
+    int pos = -1;
+    if (s < p.n_keep) {
+      if (p.identity) pos = s;
+      else if (s < p.k_pick) pos = p.sel[(size_t)u * p.cap + s];
+      else pos = p.L - p.keep_window + (s - p.k_pick);
+      if (pos < 0 || pos >= p.L) {  // never expected: keep every access in bounds
+        set_status(p.status, KVC_DEV_BAD_STATE);
+        pos = -1;
+      }
+    }
+    spos[threadIdx.x] = pos;
+    if (s < p.cap) {
+      p.pos_out[(size_t)u * p.cap + s] = pos;
+      if (p.kept) p.kept[(size_t)u * p.cap + s] = pos >= 0 ? p.votes[(size_t)u * p.L + pos] : 0.f;
+    }
+    if (blockIdx.y == 0 && threadIdx.x == 0) p.n_valid_out[u] = p.n_keep;
+  }
+  __syncthreads();
+  const int rv = p.row_vecs;
+  for (int e = threadIdx.x; e < 32 * rv; e += 256) {
+    const int r = e / rv, c = e - r * rv;
+    const int pos = spos[r];
+    if (pos < 0) continue;
+    const size_t src = ((size_t)u * p.L + pos) * rv + c;
+    const size_t dst = ((size_t)u * p.cap + r0 + r) * rv + c;
+    const uint4 kv = __ldg(p.k + src);
+    const uint4 vv = __ldg(p.v + src);
+    p.ko[dst] = kv;
+    p.vo[dst] = vv;
+  }
+}
+
+// The gather of one unit by a whole CTA, from its chosen positions spos[0..k_pick) (shared
+// memory): every cache row's position (-1 past n_keep), the kept scores, n_valid, and the
+// kept K/V rows in 16-byte pieces with eight loads in flight per thread.
+__device__ __forceinline__ void gather_unit(const GatherP &gp, int u, const int32_t *spos) {
+  const int tid = threadIdx.x;
+  // positions of every cache row (-1 past n_keep), the kept scores, n_valid
+  for (int r = tid; r < gp.cap; r += NT) {
+    int pos = -1;
+    if (r < gp.n_keep) {
+      pos = r < gp.k_pick ? spos[r] : gp.L - gp.keep_window + (r - gp.k_pick);
+      if (pos < 0 || pos >= gp.L) {  // never expected: keep every access in bounds
+        set_status(gp.status, KVC_DEV_BAD_STATE);
+        pos = -1;
+      }
+    }
+    gp.pos_out[(size_t)u * gp.cap + r] = pos;
+    if (gp.kept) gp.kept[(size_t)u * gp.cap + r] = pos >= 0 ? gp.votes[(size_t)u * gp.L + pos] : 0.f;
+  }
+  if (tid == 0) gp.n_valid_out[u] = gp.n_keep;
+  // the kept rows: 16-byte pieces, eight loads in flight per thread
+  const int rv = gp.row_vecs, rvs = rv == 16 ? 4 : 3;  // D / 8 = 16 or 8 pieces a row
+  const int total = gp.n_keep * rv;
+  for (int e0 = tid; e0 < total; e0 += 4 * NT) {
+    uint4 kk[4], vv[4];
+    size_t dst[4];
+    bool ok[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + j * NT;
+      ok[j] = e < total;
+      dst[j] = 0;
+      if (ok[j]) {
+        const int r = e >> rvs, c = e & (rv - 1);
+        const int pos = r < gp.k_pick ? spos[r] : gp.L - gp.keep_window + (r - gp.k_pick);
+        ok[j] = pos >= 0 && pos < gp.L;
+        if (ok[j]) {
+          const size_t src = ((size_t)u * gp.L + pos) * rv + c;
+          kk[j] = __ldg(gp.k + src);
+          vv[j] = __ldg(gp.v + src);
+          dst[j] = ((size_t)u * gp.cap + r) * rv + c;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (ok[j]) {
+        gp.ko[dst[j]] = kk[j];
+        gp.vo[dst[j]] = vv[j];
+      }
+  }
+}
+
 // Chunked path for long prompts (pool kernel 7): the global top-k (equal keys: lower
 // position first) lies inside the union of each chunk's local top-k taken with the same
 // rule, since restricted to one chunk it is a prefix of that chunk's order.  Kernel 1:
 // one CTA per (chunk of CHUNK_C candidates, unit) pools its range (the windows read the
 // neighbouring chunks' votes) and writes its local top-k, ascending, with their keys.
 // Kernel 2: one CTA per unit selects the top k of those candidates, which are in position
-// order chunk after chunk, and writes their positions ascending.
+// order chunk after chunk, and gathers the unit's kept rows (gather_unit).
 __global__ void __launch_bounds__(NT, 2) pool_topk_chunk_kernel(const TopkP p) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -539,7 +644,7 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_chunk_kernel(const TopkP p) {
              p.ckey + o, sm, sm + SM_KEYS, misc);
 }
 
-__global__ void __launch_bounds__(NT, 2) topk_merge_kernel(const TopkP p) {
+__global__ void __launch_bounds__(NT, 2) topk_merge_kernel(const TopkP p, const GatherP gp) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ uint32_t sm[];
@@ -627,72 +732,23 @@ __global__ void __launch_bounds__(NT, 2) topk_merge_kernel(const TopkP p) {
   for (int w2 = 0; w2 < warp; ++w2) wbase += misc[M_CSUM + w2];
   const int excl = wbase + incl - packed;
   int eq_before = excl >> 16;
+  // the chosen positions go to shared memory (the histogram region: k <= NWARP * NBIN
+  // words), then the CTA gathers the unit's rows
+  int32_t *spos = reinterpret_cast<int32_t *>(hist);
   if (gt + eq > 0) {
     int out = (excl & 0xffff) + min(eq_before, need);
-    int32_t *sel = p.sel + (size_t)u * p.cap;
 #pragma unroll
     for (int i = 0; i < RUN2; ++i) {  // branch-free: predicated stores
       const bool valid = e0 + i < total;
       const bool eqT = valid && key[i] == T;
       const bool take = (valid && key[i] > T) || (eqT && eq_before < need);
       eq_before += eqT ? 1 : 0;
-      if (take && out < p.k) sel[out] = pos[i];
+      if (take && out < p.k) spos[out] = pos[i];
       out += take ? 1 : 0;
     }
   }
-}
-
-struct GatherP {
-  const int32_t *sel;      // [U, cap] chosen prefix positions (first k)
-  const float *votes;      // [U, L] or null
-  const uint4 *k, *v;      // [U, L, D]
-  uint4 *ko, *vo;          // [U, cap, D]
-  int32_t *pos_out;        // [U, cap]
-  int32_t *n_valid_out;    // [U]
-  float *kept;             // [U, cap] or null
-  int L, cap, k_pick, n_keep, keep_window, identity, row_vecs;  // row_vecs = D / 8
-  uint32_t *status;
-};
-
-// grid (U, ceil(cap / 32)); 256 threads; each CTA fills 32 rows of one unit.
-__global__ void __launch_bounds__(256) gather_kernel(const GatherP p) {
-  // programmatic dependent launch: wait for the kernel that wrote the positions / votes
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int u = blockIdx.x;  // units on x: more than 65535 of them fit
-  const int r0 = blockIdx.y * 32;
-  __shared__ int spos[32];
-  if (threadIdx.x < 32) {
-    const int s = r0 + threadIdx.x;
-    int pos = -1;
-    if (s < p.n_keep) {
-      if (p.identity) pos = s;
-      else if (s < p.k_pick) pos = p.sel[(size_t)u * p.cap + s];
-      else pos = p.L - p.keep_window + (s - p.k_pick);
-      if (pos < 0 || pos >= p.L) {  // never expected: keep every access in bounds
-        set_status(p.status, KVC_DEV_BAD_STATE);
-        pos = -1;
-      }
-    }
-    spos[threadIdx.x] = pos;
-    if (s < p.cap) {
-      p.pos_out[(size_t)u * p.cap + s] = pos;
-      if (p.kept) p.kept[(size_t)u * p.cap + s] = pos >= 0 ? p.votes[(size_t)u * p.L + pos] : 0.f;
-    }
-    if (blockIdx.y == 0 && threadIdx.x == 0) p.n_valid_out[u] = p.n_keep;
-  }
   __syncthreads();
-  const int rv = p.row_vecs;
-  for (int e = threadIdx.x; e < 32 * rv; e += 256) {
-    const int r = e / rv, c = e - r * rv;
-    const int pos = spos[r];
-    if (pos < 0) continue;
-    const size_t src = ((size_t)u * p.L + pos) * rv + c;
-    const size_t dst = ((size_t)u * p.cap + r0 + r) * rv + c;
-    const uint4 kv = __ldg(p.k + src);
-    const uint4 vv = __ldg(p.v + src);
-    p.ko[dst] = kv;
-    p.vo[dst] = vv;
-  }
+  gather_unit(gp, u, spos);
 }
 
 // The short-prompt path (pool kernel 7, candidates in registers) with the gather fused in:
@@ -706,55 +762,11 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_gather_kernel(const TopkP p, 
   int *misc = reinterpret_cast<int *>(sm + SM_MISC);
   uint32_t *kb = sm + SM_KEYS;
   int32_t *spos = reinterpret_cast<int32_t *>(kb);  // the chosen positions [k]
-  const int u = blockIdx.x, tid = threadIdx.x;
+  const int u = blockIdx.x;
   select_run(p.votes + (size_t)u * p.L, 0, p.n_cand, p.n_cand, p.k, p.avg != 0, spos, nullptr, sm,
              kb, misc);
   __syncthreads();
-  // positions of every cache row (-1 past n_keep), the kept scores, n_valid
-  for (int r = tid; r < gp.cap; r += NT) {
-    int pos = -1;
-    if (r < gp.n_keep) {
-      pos = r < gp.k_pick ? spos[r] : gp.L - gp.keep_window + (r - gp.k_pick);
-      if (pos < 0 || pos >= gp.L) {  // never expected: keep every access in bounds
-        set_status(gp.status, KVC_DEV_BAD_STATE);
-        pos = -1;
-      }
-    }
-    gp.pos_out[(size_t)u * gp.cap + r] = pos;
-    if (gp.kept) gp.kept[(size_t)u * gp.cap + r] = pos >= 0 ? gp.votes[(size_t)u * gp.L + pos] : 0.f;
-  }
-  if (tid == 0) gp.n_valid_out[u] = gp.n_keep;
-  // the kept rows: 16-byte pieces, eight loads in flight per thread
-  const int rv = gp.row_vecs, rvs = rv == 16 ? 4 : 3;  // D / 8 = 16 or 8 pieces a row
-  const int total = gp.n_keep * rv;
-  for (int e0 = tid; e0 < total; e0 += 4 * NT) {
-    uint4 kk[4], vv[4];
-    size_t dst[4];
-    bool ok[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + j * NT;
-      ok[j] = e < total;
-      dst[j] = 0;
-      if (ok[j]) {
-        const int r = e >> rvs, c = e & (rv - 1);
-        const int pos = r < gp.k_pick ? spos[r] : gp.L - gp.keep_window + (r - gp.k_pick);
-        ok[j] = pos >= 0 && pos < gp.L;
-        if (ok[j]) {
-          const size_t src = ((size_t)u * gp.L + pos) * rv + c;
-          kk[j] = __ldg(gp.k + src);
-          vv[j] = __ldg(gp.v + src);
-          dst[j] = ((size_t)u * gp.cap + r) * rv + c;
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (ok[j]) {
-        gp.ko[dst[j]] = kk[j];
-        gp.vo[dst[j]] = vv[j];
-      }
-  }
+  gather_unit(gp, u, spos);
 }
 
 bool g_topk_attr[64];
@@ -864,8 +876,7 @@ cudaError_t launch_select_gather(const Ctx &c, const SelectArgs &a) {
       if (e != cudaSuccess) return e;
       cfg.gridDim = dim3((unsigned)a.units);
       cfg.dynamicSmemBytes = (size_t)SM_KEYS * 4;
-      e = cudaLaunchKernelEx(&cfg, topk_merge_kernel, tp);
-      if (e != cudaSuccess) return e;
+      return cudaLaunchKernelEx(&cfg, topk_merge_kernel, tp, gp);  // with the gather
     } else {
       cfg.gridDim = dim3((unsigned)a.units);
       cfg.dynamicSmemBytes = (size_t)smem;
