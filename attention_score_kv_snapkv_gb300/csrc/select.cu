@@ -123,15 +123,17 @@ __device__ __forceinline__ void find_bin(const uint32_t *hist, int *misc, int ne
   __syncthreads();
 }
 
-// The pool-kernel-7 path with each thread's keys in registers: pooled keys of the
-// candidates [c0, c0 + nc) of a unit whose votes v hold nall candidates (the windows read
-// up to three positions beyond the range where those exist, else the padding), then the
+// The pool-kernel-7 (or pool-kernel-1: nopool) path with each thread's keys in registers:
+// pooled keys of the candidates [c0, c0 + nc) of a unit whose votes v hold nall candidates
+// (the windows read up to three positions beyond the range where those exist, else the
+// padding), then the
 // positions of the k largest (equal keys: lower position first), ascending, into
 // sel_out[0..k) and, with key_out, their keys beside them.  nc <= NT * RUN, 1 <= k <= nc.
 // Shared memory: the histogram region, misc, and key_words(nc) words at `stage`.
 __device__ __forceinline__ void select_run(const float *v, int c0, int nc, int nall, int k,
-                                           bool avg, int32_t *sel_out, uint32_t *key_out,
-                                           uint32_t *sm, uint32_t *stage, int *misc) {
+                                           bool avg, bool nopool, int32_t *sel_out,
+                                           uint32_t *key_out, uint32_t *sm, uint32_t *stage,
+                                           int *misc) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float pad = avg ? 0.f : -INFINITY;  // value beyond both ends of the candidates
   const float inv = 1.f / 7.f;
@@ -202,8 +204,9 @@ __device__ __forceinline__ void select_run(const float *v, int c0, int nc, int n
     }
 #pragma unroll
     for (int i = 0; i < RUN; ++i) {
-      const float m = avg ? (((((w[i] + w[i + 1]) + w[i + 2]) + w[i + 3]) + w[i + 4]) + w[i + 5] + w[i + 6]) * inv
-                          : fmax3(fmax3(w[i], w[i + 1], w[i + 2]), fmax3(w[i + 3], w[i + 4], w[i + 5]), w[i + 6]);
+      const float m = nopool ? w[i + 3]
+                      : avg ? (((((w[i] + w[i + 1]) + w[i + 2]) + w[i + 3]) + w[i + 4]) + w[i + 5] + w[i + 6]) * inv
+                            : fmax3(fmax3(w[i], w[i + 1], w[i + 2]), fmax3(w[i + 3], w[i + 4], w[i + 5]), w[i + 6]);
       key[i] = j0 + i < nc ? order_key(m) : 0u;
     }
   }
@@ -640,7 +643,8 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_chunk_kernel(const TopkP p) {
   const int c0 = c * CHUNK_C;
   const int nc = min(CHUNK_C, p.n_cand - c0);
   const size_t o = ((size_t)u * p.nchunks + c) * p.cap;
-  select_run(p.votes + (size_t)u * p.L, c0, nc, p.n_cand, min(p.k, nc), p.avg != 0, p.cpos + o,
+  select_run(p.votes + (size_t)u * p.L, c0, nc, p.n_cand, min(p.k, nc), p.avg != 0, p.half == 0,
+             p.cpos + o,
              p.ckey + o, sm, sm + SM_KEYS, misc);
 }
 
@@ -763,8 +767,8 @@ __global__ void __launch_bounds__(NT, 2) pool_topk_gather_kernel(const TopkP p, 
   uint32_t *kb = sm + SM_KEYS;
   int32_t *spos = reinterpret_cast<int32_t *>(kb);  // the chosen positions [k]
   const int u = blockIdx.x;
-  select_run(p.votes + (size_t)u * p.L, 0, p.n_cand, p.n_cand, p.k, p.avg != 0, spos, nullptr, sm,
-             kb, misc);
+  select_run(p.votes + (size_t)u * p.L, 0, p.n_cand, p.n_cand, p.k, p.avg != 0, p.half == 0, spos,
+             nullptr, sm, kb, misc);
   __syncthreads();
   gather_unit(gp, u, spos);
 }
@@ -847,9 +851,10 @@ cudaError_t launch_select_gather(const Ctx &c, const SelectArgs &a) {
     cfg.numAttrs = 1;
     // long prompts with pool kernel 7: the chunked path when the chunks' candidates fit
     // the merge's registers
-    const bool chunked = tp.half == 3 && n_cand > CHUNK_C && tp.nchunks * k_pick <= NT * RUN2;
-    // short prompts with pool kernel 7: selection and gather in one kernel
-    const bool fused = tp.half == 3 && n_cand <= CHUNK_C && (a.D == 64 || a.D == 128);
+    const bool reg_pool = tp.half == 3 || tp.half == 0;  // pool kernel 7 or 1
+    const bool chunked = reg_pool && n_cand > CHUNK_C && tp.nchunks * k_pick <= NT * RUN2;
+    // short prompts with pool kernel 7 or 1: selection and gather in one kernel
+    const bool fused = reg_pool && n_cand <= CHUNK_C && (a.D == 64 || a.D == 128);
     if (fused) {
       if (dev < 64 && !g_fused_attr[dev]) {
         cudaError_t e = cudaFuncSetAttribute(pool_topk_gather_kernel,

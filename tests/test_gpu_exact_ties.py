@@ -6,8 +6,8 @@
   here are multiples of 1/4 below 3, so every pooled value (a maximum, or a window sum
   of such multiples, which fp32 forms exactly) is exact in fp32 and in fp64: the
   oracle's fp64 selection is then the only correct answer, and the GPU's must equal it.
-  Each case runs one of the selection kernels' radix paths: pool 7 with the candidates
-  in registers; pool 7 over more than 16384 candidates in chunks of 16384 (each chunk's
+  Each case runs one of the selection kernels' radix paths: pool 7 (or 1) with the
+  candidates in registers; pool 7 (or 1) over more than 16384 candidates in chunks of 16384 (each chunk's
   local top-k, then their merge; the plateaus straddle the chunk boundaries); keys in
   shared memory (other pool sizes, or chunks whose candidates exceed the merge's 8192);
   keys in global memory (more than 49152 candidates); unaligned vote rows take the
@@ -36,7 +36,9 @@ SELECT_CASES = [
     ("registers-max7-16384", 16384, 32, 7, 2400, False),
     ("registers-avg7", 4096, 32, 7, 480, True),
     ("shared-max5", 3000, 16, 5, 300, False),
-    ("shared-max1", 5000, 8, 1, 700, False),
+    ("registers-max1", 5000, 8, 1, 700, False),
+    ("chunked-max1-40000", 40000, 8, 1, 2000, False),
+    ("shared-max1-20000", 20000, 8, 1, 5000, False),
     ("shared-max7-20000", 20000, 32, 7, 5000, False),
     ("chunked-max7-20000", 20000, 32, 7, 3000, False),
     ("chunked-avg7-40000", 40000, 32, 7, 992, True),
