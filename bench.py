@@ -1175,7 +1175,8 @@ def run_ours(args):
                               "algorithmic_bytes": compress_bytes(),
                               "traffic": compress_traffic(),
                               "traffic_source": "profiles/compress_traffic.json (ncu dram bytes of "
-                                                "the three launches of one %d-layer compression)" % LY},
+                                                "the launches of one %d-layer compression: the window vote, then the fused "
+                                                "selection and gather)" % LY},
         "gpu_launches": args.steps * (3 + STEPS),
         "device_status": status,
         "clocks": clk,
