@@ -1211,6 +1211,16 @@ def run_ours(args):
                             if k2 in ("n_sink", "ring", "step_ms", "step_GBps",
                                       "step_frac_of_hbm_peak", "device_status")}
                            for S in (0, 1, 2, 4, 8)]}
+        # the same compression when the prefill (prefill_attention_lse) supplies each row's
+        # log-sum-exp: snapkv_votes_from_lse + snapkv_select (aux.lse_route); a second
+        # route, not the headline value, which times snapkv_compress alone
+        lr = line["aux"]["lse_route"]["snapkv"]
+        line["compress_from_lse"] = {
+            "ms": lr["compress_from_lse_ms"],
+            "prefix_tokens_per_s": lr["compress_from_lse_prefix_tokens_per_s"],
+            "GBps": compress_bytes() / (lr["compress_from_lse_ms"] / 1e3) / 1e9,
+            "frac_of_hbm_peak": compress_bytes() / (lr["compress_from_lse_ms"] / 1e3) / 1e9 / hbm_peak,
+            "entry_points": "snapkv_votes_from_lse + snapkv_select, given the rows' log-sum-exp"}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
