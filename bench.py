@@ -83,15 +83,16 @@ def decode_traffic(rows_per_launch_avg):
 
 
 def compress_traffic():
-    """dram read + write bytes of one compression of all layers (window vote, pool/top-k
-    and gather launches) from the committed ncu capture; None if the kernel sources
-    changed since the capture or the layer count differs."""
+    """dram read + write bytes of one compression of all layers (the two-pass window vote,
+    then the fused selection and gather: the kernels this workload launches) from the
+    committed ncu capture; None if those kernels' sources changed since the capture or
+    the layer count differs."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "compress_traffic.json")) as f:
             j = json.load(f)
         h = hashlib.sha256()
-        for name in ("window_vote.cu", "window_vote_tmem.cu", "select.cu", "kvc_internal.cuh"):
+        for name in j["sources"]:
             with open(os.path.join(ROOT, "attention_score_kv_snapkv_gb300", "csrc", name), "rb") as f:
                 h.update(f.read())
         if h.hexdigest() != j["sources_sha256"] or j["units"] != UNITS:
