@@ -817,9 +817,11 @@ def measure_stream(kvc, WL, dev, hbm_peak, steps=256, n_sink=None, ring=None):
 
 
 def run_host_link(args):
-    """Host-link copy rates behind the end-to-end number (printed as one JSON line): 2 GiB
+    """Host-link rates behind the end-to-end number (printed as one JSON line): 2 GiB
     from pinned host memory to the device over 1, 2, 4 and 8 streams, the same as 64 MB
-    copies on one stream, and 2 GiB device to pinned host; best of three, CUDA events."""
+    copies on one stream, and 2 GiB device to pinned host (best of three, CUDA events);
+    then the library's gather reading 128 MiB of V rows in place from pinned host memory
+    (SM loads over the link, checked against the rows)."""
     import torch
 
     n = 2 * 1024 ** 3
@@ -860,6 +862,38 @@ def run_host_link(args):
             d[i:i + c].copy_(h[i:i + c], non_blocking=True)
     res["h2d_GBps_64MB_copies_one_stream"] = best(h2d_chunks)
     res["d2h_GBps"] = best(lambda: h.copy_(d, non_blocking=True))
+    del h, d
+    # SM loads over the same link: the library's gather reading a pinned host V in place
+    # (snapkv_select with a budget covering the prompt keeps every row: 8 units x 65536
+    # rows x 256 B of V from the host, K from the device)
+    import attention_score_kv_snapkv_gb300 as kvc
+    L = 65536
+    kd = torch.randn((1, 1, 8, L, 128), device="cuda").to(torch.bfloat16)
+    vh = torch.empty((1, 1, 8, L, 128), dtype=torch.bfloat16).pin_memory()
+    vh.copy_(kd.cpu())
+    vd = vh.to("cuda")
+    votes = torch.zeros((1, 1, 8, L), dtype=torch.float32, device="cuda")
+    vbytes = vh.numel() * vh.element_size()
+
+    def gather_rate(v):
+        ms = []
+        for _ in range(4):
+            torch.cuda.synchronize()
+            a, b = ev(), ev()
+            a.record(cur)
+            r = kvc.snapkv_select(votes, kd, v, keep_window=32, pool_kernel=7, budget=L)
+            b.record(cur)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        assert torch.equal(r["v"], vd), "gathered rows differ from the input rows"
+        return min(ms[1:])
+
+    t_host, t_dev = gather_rate(vh), gather_rate(vd)
+    res["gather_v_bytes"] = vbytes
+    res["gather_host_v_ms"] = t_host
+    res["gather_device_v_ms"] = t_dev
+    res["gather_host_v_GBps"] = vbytes / (t_host / 1e3) / 1e9
+    res["device_status"] = kvc.kvc_device_status()
     print(json.dumps({"host_link": res}), flush=True)
     return 0
 
