@@ -1,10 +1,18 @@
-"""GPU parity of snapkv_compress on seeded random shapes: head dim, head grouping (any G
-up to 8), prompt length (1 to 20000 tokens, so every selection path and window-vote
-kernel is reached), window, pool kernel, max or average pooling and budget (from keeping
-only the window to keeping everything) are drawn from a fixed list of seeds, and every
-call is checked against the fp64 oracle with the shared parity rules: votes within 1e-5
-relative, kept sets identical up to swaps inside the tie band, window positions appended
-in order, and the compact cache holding exactly the rows at the reported positions."""
+"""GPU parity on seeded random shapes, against the fp64 oracle with the shared parity
+rules.
+
+* snapkv_compress: head dim, head grouping (any G up to 8), prompt length (1 to 20000
+  tokens, so every selection path and window-vote kernel is reached), window, pool
+  kernel, max or average pooling and budget (from keeping only the window to keeping
+  everything): votes within 1e-5 relative, kept sets identical up to swaps inside the tie
+  band, window positions appended in order, the compact cache holding exactly the rows
+  at the reported positions.
+* snapkv_votes_from_lse: head dim, grouping, prompt length and voting rows (from one
+  query to every prompt query), given each row's log-sum-exp shifted by up to 0.5 and
+  NaN at every position the kernel must not read: votes within 1e-5 relative.
+* compressed_decode_attn with the fused append: layers, batch, KV heads, grouping, head
+  dim, capacity and ragged row counts: appended rows, row counts and outputs (2e-2
+  absolute + 1e-2 relative)."""
 
 import dataclasses
 
@@ -13,8 +21,9 @@ import pytest
 import torch
 
 import workloads as W
+from oracle import attention as OA
 from oracle import snapkv as OS
-from parity import assert_votes_close, check_selected_set, f64
+from parity import assert_outputs_close, assert_votes_close, check_selected_set, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -91,3 +100,106 @@ def test_random_shape_matches_oracle(kvc, shape):
             assert torch.equal(kc[0, b, h, :n_keep], x["K"][0, b, h, idx])
             assert torch.equal(vc[0, b, h, :n_keep], x["V"][0, b, h, idx])
     assert swaps <= max(1, B * Hkv // 4)
+
+
+def draw_vote_shape(seed):
+    """(name, batch, layers, Hq, Hkv, D, L, Wq) for one seed; G * Wq * L stays small
+    enough for the oracle."""
+    r = np.random.RandomState(seed)
+    D = int(r.choice([64, 128]))
+    Hkv = int(r.choice([1, 2]))
+    G = int(r.randint(1, 9))
+    L = max(1, int(np.exp(r.uniform(0.0, np.log(2500.0)))))
+    if r.rand() < 0.25:
+        Wq = L                                     # every prompt query votes (H2O)
+    else:
+        Wq = int(r.randint(1, min(L, 96) + 1))
+    while G * Wq * L > 4_000_000 and Wq > 1:
+        Wq //= 2
+    B = int(r.choice([1, 2]))
+    name = "seed%d-D%d-G%d-Hkv%d-L%d-Wq%d" % (seed, D, G, Hkv, L, Wq)
+    return (name, B, 1, G * Hkv, Hkv, D, L, Wq)
+
+
+VOTE_SHAPES = [draw_vote_shape(s) for s in range(201, 213)]
+
+
+@pytest.mark.parametrize("shape", VOTE_SHAPES, ids=[s[0] for s in VOTE_SHAPES])
+def test_random_shape_votes_from_lse(kvc, shape):
+    name, B, Ly, Hq, Hkv, D, L, Wq = shape
+    G = Hq // Hkv
+    g = torch.Generator().manual_seed(L * 31 + Wq)
+    q = torch.randn((Ly, B, Hq, Wq, D), generator=g).to(torch.bfloat16)
+    k = torch.randn((Ly, B, Hkv, L, D), generator=g).to(torch.bfloat16)
+    qh, kh = f64(q), f64(k)
+    rng = np.random.default_rng(L + Wq)
+    lse = np.full((Ly, B, Hq, L), np.nan)          # positions before the window: never read
+    for b in range(B):
+        for hq in range(Hq):
+            for r in range(Wq):
+                pos = L - Wq + r
+                lse[0, b, hq, pos] = (OA.log_sum_exp(kh[0, b, hq // G, :pos + 1] @ qh[0, b, hq, r]
+                                                     / np.sqrt(D)) + rng.uniform(-0.5, 0.5))
+    dev = torch.device("cuda")
+    lse_d = torch.as_tensor(lse, dtype=torch.float32).to(dev)
+    votes = kvc.snapkv_votes_from_lse(q.to(dev), k.to(dev), lse_d)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    vg = votes.cpu().numpy()
+    lse32 = lse_d.double().cpu().numpy()            # the normalisers the kernel was given
+    for b in range(B):
+        for h in range(Hkv):
+            ref = OS.votes_from_lse(qh[0, b, h * G:(h + 1) * G], kh[0, b, h],
+                                    lse32[0, b, h * G:(h + 1) * G])
+            assert_votes_close(vg[0, b, h], ref, "%s votes (%d,%d)" % (name, b, h))
+
+
+def draw_decode_shape(seed):
+    """(name, layers, batch, Hq, Hkv, D, cap) for one seed."""
+    r = np.random.RandomState(seed)
+    D = int(r.choice([64, 128]))
+    Hkv = int(r.randint(1, 9))
+    G = int(r.randint(1, 9))
+    Ly = int(r.choice([1, 2]))
+    B = int(r.randint(1, 5))
+    cap = max(2, int(np.exp(r.uniform(np.log(2.0), np.log(3000.0)))))
+    name = "seed%d-Ly%d-B%d-G%d-Hkv%d-D%d-cap%d" % (seed, Ly, B, G, Hkv, D, cap)
+    return (name, Ly, B, G * Hkv, Hkv, D, cap)
+
+
+DECODE_SHAPES = [draw_decode_shape(s) for s in range(301, 313)]
+
+
+@pytest.mark.parametrize("shape", DECODE_SHAPES, ids=[s[0] for s in DECODE_SHAPES])
+def test_random_shape_decode_with_append(kvc, shape):
+    name, Ly, B, Hq, Hkv, D, cap = shape
+    G = Hq // Hkv
+    g = torch.Generator().manual_seed(cap * 13 + Hq)
+    q = torch.randn((Ly, B, Hq, D), generator=g).to(torch.bfloat16)
+    kc = torch.randn((Ly, B, Hkv, cap, D), generator=g).to(torch.bfloat16)
+    vc = torch.randn((Ly, B, Hkv, cap, D), generator=g).to(torch.bfloat16)
+    kn = torch.randn((Ly, B, Hkv, D), generator=g).to(torch.bfloat16)
+    vn = torch.randn((Ly, B, Hkv, D), generator=g).to(torch.bfloat16)
+    n0 = torch.randint(0, cap, (Ly, B, Hkv), generator=g, dtype=torch.int32)
+    n0.view(-1)[0] = cap - 1                        # a unit the append fills
+    dev = torch.device("cuda")
+    kcd, vcd, nd = kc.to(dev), vc.to(dev), n0.to(dev)
+    out = kvc.compressed_decode_attn(q.to(dev), kcd, vcd, n_valid=nd, k_new=kn.to(dev),
+                                     v_new=vn.to(dev))
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    kc2, vc2 = kc.clone(), vc.clone()
+    for idx in np.ndindex(*n0.shape):
+        kc2[idx + (int(n0[idx]),)] = kn[idx]
+        vc2[idx + (int(n0[idx]),)] = vn[idx]
+    assert torch.equal(nd.cpu(), n0 + 1)
+    assert torch.equal(kcd.cpu(), kc2) and torch.equal(vcd.cpu(), vc2)
+    qh, kh, vh = f64(q), f64(kc2), f64(vc2)
+    ref = np.zeros_like(qh)
+    for ly in range(Ly):
+        for b in range(B):
+            for h in range(Hkv):
+                m = int(n0[ly, b, h]) + 1
+                ref[ly, b, h * G:(h + 1) * G] = OA.attend_group(qh[ly, b, h * G:(h + 1) * G],
+                                                                kh[ly, b, h, :m], vh[ly, b, h, :m])
+    assert_outputs_close(f64(out), ref, name)
