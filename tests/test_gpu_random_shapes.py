@@ -12,7 +12,12 @@ rules.
   NaN at every position the kernel must not read: votes within 1e-5 relative.
 * compressed_decode_attn with the fused append: layers, batch, KV heads, grouping, head
   dim, capacity and ragged row counts: appended rows, row counts and outputs (2e-2
-  absolute + 1e-2 relative)."""
+  absolute + 1e-2 relative).
+* H2O: head dim, grouping, prompt length, heavy and recent budgets (either may be small,
+  the heavy one zero) and enough decode steps that decode-appended tokens become eviction
+  candidates, in lockstep with the oracle (prefill cut and scores, then every step's
+  output, evicted position, live set and cumulative scores), whichever of the one-CTA and
+  split step kernels the shape gets."""
 
 import dataclasses
 
@@ -24,6 +29,7 @@ import workloads as W
 from oracle import attention as OA
 from oracle import snapkv as OS
 from parity import assert_outputs_close, assert_votes_close, check_selected_set, f64
+from test_gpu_h2o_sink import run_h2o_lockstep
 
 pytestmark = pytest.mark.gpu
 
@@ -203,3 +209,32 @@ def test_random_shape_decode_with_append(kvc, shape):
                 ref[ly, b, h * G:(h + 1) * G] = OA.attend_group(qh[ly, b, h * G:(h + 1) * G],
                                                                 kh[ly, b, h, :m], vh[ly, b, h, :m])
     assert_outputs_close(f64(out), ref, name)
+
+
+def draw_h2o_shape(seed):
+    """(name, layers, batch, Hq, Hkv, D, L, n_heavy, n_recent, steps) for one seed."""
+    r = np.random.RandomState(seed)
+    D = int(r.choice([64, 128]))
+    Hkv = int(r.choice([1, 2]))
+    G = int(r.randint(1, 9))
+    B = int(r.choice([1, 2]))
+    n_heavy = int(r.randint(1, 200))
+    if seed % 4 == 1:
+        n_heavy = 0                                # recent window only: a sliding window
+    n_recent = int(r.randint(1, 40))
+    L = int(r.randint(max(1, n_heavy + n_recent - 8), n_heavy + n_recent + 400))
+    steps = n_recent + int(r.randint(2, 10))
+    name = "seed%d-D%d-G%d-Hkv%d-B%d-L%d-heavy%d-recent%d-steps%d" % (seed, D, G, Hkv, B, L,
+                                                                     n_heavy, n_recent, steps)
+    return (name, 1, B, G * Hkv, Hkv, D, L, n_heavy, n_recent, steps)
+
+
+H2O_SHAPES = [draw_h2o_shape(s) for s in range(401, 409)]
+
+
+@pytest.mark.parametrize("shape", H2O_SHAPES, ids=[s[0] for s in H2O_SHAPES])
+def test_random_shape_h2o_lockstep(kvc, shape):
+    name, Ly, B, Hq, Hkv, D, L, n_heavy, n_recent, steps = shape
+    swaps = run_h2o_lockstep(kvc, Ly, B, Hq, Hkv, D, L, n_heavy, n_recent, steps,
+                             seed=L + 7 * n_heavy + n_recent)
+    assert swaps <= 2
