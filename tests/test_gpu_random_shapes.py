@@ -17,7 +17,11 @@ rules.
   the heavy one zero) and enough decode steps that decode-appended tokens become eviction
   candidates, in lockstep with the oracle (prefill cut and scores, then every step's
   output, evicted position, live set and cumulative scores), whichever of the one-CTA and
-  split step kernels the shape gets."""
+  split step kernels the shape gets.
+* StreamingLLM: sink count (0 = plain window attention), ring size, grouping and head dim,
+  streamed past the ring at least twice: the attention after every append against the
+  oracle's sink + ring cache on sampled steps (every step until the ring first wraps),
+  and the final slot positions."""
 
 import dataclasses
 
@@ -28,6 +32,7 @@ import torch
 import workloads as W
 from oracle import attention as OA
 from oracle import snapkv as OS
+from oracle import streaming as OSt
 from parity import assert_outputs_close, assert_votes_close, check_selected_set, f64
 from test_gpu_h2o_sink import run_h2o_lockstep
 
@@ -238,3 +243,52 @@ def test_random_shape_h2o_lockstep(kvc, shape):
     swaps = run_h2o_lockstep(kvc, Ly, B, Hq, Hkv, D, L, n_heavy, n_recent, steps,
                              seed=L + 7 * n_heavy + n_recent)
     assert swaps <= 2
+
+
+def draw_sink_shape(seed):
+    """(name, batch, Hq, Hkv, D, n_sink, ring, stream length) for one seed."""
+    r = np.random.RandomState(seed)
+    D = int(r.choice([64, 128]))
+    Hkv = int(r.choice([1, 2, 3]))
+    G = int(r.randint(1, 9))
+    B = int(r.choice([1, 2]))
+    S = int(r.randint(0, 9))
+    R = max(1, int(np.exp(r.uniform(0.0, np.log(300.0)))))
+    T = S + 2 * R + int(r.randint(1, 40))
+    name = "seed%d-D%d-G%d-Hkv%d-B%d-sinks%d-ring%d-T%d" % (seed, D, G, Hkv, B, S, R, T)
+    return (name, B, G * Hkv, Hkv, D, S, R, T)
+
+
+SINK_SHAPES = [draw_sink_shape(s) for s in range(501, 507)]
+
+
+@pytest.mark.parametrize("shape", SINK_SHAPES, ids=[s[0] for s in SINK_SHAPES])
+def test_random_shape_sink_ring(kvc, shape):
+    name, B, Hq, Hkv, D, S, R, T = shape
+    G = Hq // Hkv
+    dev = torch.device("cuda")
+    kc = torch.zeros((1, B, Hkv, S + R, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    pos = torch.full((1, B, Hkv, S + R), -1, dtype=torch.int32, device=dev)
+    caches = {(b, h): OSt.SinkCache(S, R, D) for b in range(B) for h in range(Hkv)}
+    g = torch.Generator().manual_seed(S * 1000 + R)
+    for t in range(T):
+        q = torch.randn((1, B, Hq, D), generator=g).to(torch.bfloat16)
+        k = torch.randn((1, B, Hkv, D), generator=g).to(torch.bfloat16)
+        v = torch.randn((1, B, Hkv, D), generator=g).to(torch.bfloat16)
+        kvc.sink_window_append(k.to(dev), v.to(dev), kc, vc, t, n_sink=S, n_recent=R, pos=pos)
+        out = kvc.compressed_decode_attn(q.to(dev), kc, vc, n_uniform=min(t + 1, S + R))
+        kh, vh = f64(k), f64(v)
+        for (b, h), c in caches.items():
+            c.append(t, kh[0, b, h], vh[0, b, h])
+        if t <= S + R + 2 or t % 5 == 0 or t == T - 1:
+            outh, qh = f64(out), f64(q)
+            for (b, h), c in caches.items():
+                ref = c.attend(qh[0, b, h * G:(h + 1) * G], t)
+                assert_outputs_close(outh[0, b, h * G:(h + 1) * G], ref, "%s step %d" % (name, t))
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    p = pos.cpu().numpy()
+    for b in range(B):
+        for h in range(Hkv):
+            assert sorted(p[0, b, h].tolist()) == sorted(OSt.visible_positions(T - 1, S, R).tolist())
