@@ -18,6 +18,8 @@ rules.
   candidates, in lockstep with the oracle (prefill cut and scores, then every step's
   output, evicted position, live set and cumulative scores), whichever of the one-CTA and
   split step kernels the shape gets.
+* prefill_attention_lse: head dim, grouping and prompt length (1 to 1500 tokens): every
+  row's log-sum-exp (2e-5 absolute) and the attention output of sampled heads.
 * StreamingLLM: sink count (0 = plain window attention), ring size, grouping and head dim,
   streamed past the ring at least twice: the attention after every append against the
   oracle's sink + ring cache on sampled steps (every step until the ring first wraps),
@@ -292,3 +294,45 @@ def test_random_shape_sink_ring(kvc, shape):
     for b in range(B):
         for h in range(Hkv):
             assert sorted(p[0, b, h].tolist()) == sorted(OSt.visible_positions(T - 1, S, R).tolist())
+
+
+def draw_prefill_shape(seed):
+    """(name, batch, Hq, Hkv, D, L) for one seed."""
+    r = np.random.RandomState(seed)
+    D = int(r.choice([64, 128]))
+    Hkv = int(r.choice([1, 2]))
+    G = int(r.randint(1, 5))
+    B = int(r.choice([1, 2]))
+    if seed % 2:                                   # several key tiles, ragged last one
+        L = int(r.randint(129, 1501))
+    else:
+        L = max(1, int(np.exp(r.uniform(0.0, np.log(1500.0)))))
+    name = "seed%d-D%d-G%d-Hkv%d-B%d-L%d" % (seed, D, G, Hkv, B, L)
+    return (name, B, G * Hkv, Hkv, D, L)
+
+
+PREFILL_SHAPES = [draw_prefill_shape(s) for s in range(601, 607)]
+
+
+@pytest.mark.parametrize("shape", PREFILL_SHAPES, ids=[s[0] for s in PREFILL_SHAPES])
+def test_random_shape_prefill_lse(kvc, shape):
+    name, B, Hq, Hkv, D, L = shape
+    G = Hq // Hkv
+    g = torch.Generator().manual_seed(L * 7 + Hq)
+    q = torch.randn((1, B, Hq, L, D), generator=g).to(torch.bfloat16)
+    k = torch.randn((1, B, Hkv, L, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((1, B, Hkv, L, D), generator=g).to(torch.bfloat16)
+    dev = torch.device("cuda")
+    out, lse = kvc.prefill_attention_lse(q.to(dev), k.to(dev), v.to(dev))
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status() == 0
+    qh, kh, vh = f64(q), f64(k), f64(v)
+    lg = lse.double().cpu().numpy()
+    for b in range(B):
+        for hq in range(Hq):
+            h = hq // G
+            err = np.abs(lg[0, b, hq] - OA.causal_lse(qh[0, b, hq], kh[0, b, h])).max()
+            assert err <= 2e-5, (name, b, hq, err)
+            if hq % G == 0:  # one query head of each group
+                ref = OA.causal_prefill(qh[0, b, hq], kh[0, b, h], vh[0, b, h])
+                assert_outputs_close(f64(out[0, b, hq]), ref, "%s output (%d,%d)" % (name, b, hq))
