@@ -11,4 +11,5 @@ from ._binding import (  # noqa: F401
     h2o_decode_step, h2o_prefill, h2o_prefill_from_votes, h2o_step_ctas_per_unit,
     kvc_device_status, kvc_selftest_wait_timeout, kvc_set_wait_timeout_ns, kvc_version, lib,
     library_path, prefill_attention_lse, sink_window_append, snapkv_compress,
-    snapkv_prefill_attention, snapkv_select, snapkv_votes_from_lse, snapkv_workspace_bytes)
+    snapkv_prefill_attention, snapkv_select, snapkv_vote_plan, snapkv_votes_from_lse,
+    snapkv_workspace_bytes)

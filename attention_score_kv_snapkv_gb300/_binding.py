@@ -66,6 +66,8 @@ _SIGS = {
     "kvc_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "kvc_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, _P]),
     "snapkv_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(SnapKVParams)]),
+    "snapkv_vote_plan": (ctypes.c_int, [ctypes.POINTER(SnapKVParams), ctypes.c_int32,
+                                        ctypes.POINTER(ctypes.c_int64)]),
     "snapkv_compress": (ctypes.c_int, [ctypes.POINTER(SnapKVParams), _P, _P, _P, _P, _P, _P, _P,
                                        _P, _P, _P, ctypes.c_size_t, _P]),
     "snapkv_select": (ctypes.c_int, [ctypes.POINTER(SnapKVParams), _P, _P, _P, _P, _P, _P, _P, _P,
@@ -204,6 +206,21 @@ def snapkv_params(q_win, k, n_query, keep_window, pool_kernel, budget, cap, pool
 
 def snapkv_workspace_bytes(params):
     return lib().snapkv_workspace_bytes(ctypes.byref(params))
+
+
+def snapkv_vote_plan(n_layers, batch, n_q_heads, n_kv_heads, head_dim, prompt_len, n_query,
+                     keep_window, pool_kernel, budget, cap=None, pool_avg=False, num_sms=0):
+    """The window-vote plan snapkv_compress uses for these sizes on a GPU with num_sms SMs
+    (0: the current device's): a dict with single (1: the single-pass kernel, 0: two
+    passes), g (CTAs per job), groups, row_tiles, rows_per_tile and exchange_bytes.  No
+    device is needed.  Raises KVCError where snapkv_compress would reject the sizes."""
+    cap = budget if cap is None else cap
+    p = SnapKVParams(n_layers, batch, n_q_heads, n_kv_heads, head_dim, prompt_len, n_query,
+                     keep_window, pool_kernel, budget, cap, 1 if pool_avg else 0)
+    out = (ctypes.c_int64 * 6)()
+    _check(lib().snapkv_vote_plan(ctypes.byref(p), num_sms, out), "snapkv_vote_plan")
+    keys = ("single", "g", "groups", "row_tiles", "rows_per_tile", "exchange_bytes")
+    return {k: int(v) for k, v in zip(keys, out)}
 
 
 def snapkv_compress(q_win, k, v, *, keep_window, pool_kernel, budget, cap=None, k_out=None,

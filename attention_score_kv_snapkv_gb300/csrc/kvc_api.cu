@@ -458,6 +458,22 @@ size_t snapkv_workspace_bytes(const kvc_snapkv_params *p) {
   return s.total > 0 ? s.total : 256;
 }
 
+kvc_status snapkv_vote_plan(const kvc_snapkv_params *p, int32_t num_sms, int64_t *out) {
+  if (!p || !out) return KVC_ERR_NULL;
+  const int sms = num_sms > 0 ? num_sms : sms_for_sizing();
+  SnapPlan s;
+  const kvc_status st = plan_snapkv(p, true, sms, &s);
+  if (st != KVC_OK) return st;
+  const WindowVotePlan pl = plan_window_vote((int)s.units, p->prompt_len, s.R, p->n_query, sms);
+  out[0] = pl.single;
+  out[1] = pl.g;
+  out[2] = pl.ngroups;
+  out[3] = pl.row_tiles;
+  out[4] = pl.qr;
+  out[5] = (int64_t)pl.ws_bytes;
+  return KVC_OK;
+}
+
 kvc_status snapkv_compress(const kvc_snapkv_params *p, const void *q_win, const void *k,
                            const void *v, void *k_out, void *v_out, int32_t *pos_out,
                            int32_t *n_valid_out, float *votes_out, float *kept_scores_out,

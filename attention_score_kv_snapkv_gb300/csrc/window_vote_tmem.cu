@@ -713,7 +713,11 @@ bool g_attr_done[8][64];
 // least MIN_TPC tiles to stream meanwhile.  Measured on GB300: with 128 query rows per
 // job (NB = 4) neither holds and the two-pass kernel is faster.  Among the group sizes
 // that qualify, a round (every group on one job) costs about the busiest CTA's key
-// tiles, plus its Q tile (qr/128 of a key tile) and, when g > 1, the exchange.
+// tiles, plus its Q tile (qr/128 of a key tile) and, when g > 1, the exchange.  Of equal
+// costs the smallest g is taken: its CTAs' shares are the most even.  Measured on the
+// long-context prompt (1024 key tiles per job, 8 layers): g = 147 (7 tiles on all but 4
+// CTAs) 1.82 ms, against 1.99 ms for g = 152 (6 or 7 tiles), 1.96 ms for g = 128 (8
+// each, tensor memory full with two jobs) and 2.16 ms for g = 140.
 constexpr int MIN_TPC = 4;
 bool plan_window_vote_tmem(int units, int L, int R, int Wq, int num_sms, WindowVotePlan *pl) {
   const int row_tiles = (R + TILE - 1) / TILE;

@@ -118,6 +118,21 @@ typedef struct {
 /* Bytes of device workspace snapkv_compress needs for *p (0 is never returned). */
 size_t snapkv_workspace_bytes(const kvc_snapkv_params *p);
 
+/* The plan of the window votes (SnapKV article, 処理の流れ steps 1-2) that snapkv_compress
+ * uses for *p on a GPU with num_sms SMs (num_sms <= 0: the current device's count, or 160
+ * without one).  Host-only: no device is needed and nothing is launched; for diagnostics
+ * and for callers that check which kernel runs.  On KVC_OK, out (host, 6 entries) holds:
+ *   out[0] 1 for the single-pass kernel (each CTA's scores held in tensor memory until the
+ *          rows' statistics are known), 0 for the two-pass kernel;
+ *   out[1] CTAs per job (the group size g; a job is a unit's tile of query rows);
+ *   out[2] groups (num_sms / g; CTAs past the last whole group stay idle);
+ *   out[3] row tiles per unit; out[4] query rows per tile;
+ *   out[5] bytes of the groups' statistics-exchange records within the workspace.
+ * The votes are formed unless the call keeps every position and asks for no votes.
+ * Returns KVC_ERR_NULL, KVC_ERR_SHAPE or KVC_ERR_BUDGET where snapkv_compress would reject
+ * *p with that code (out untouched), else KVC_OK. */
+kvc_status snapkv_vote_plan(const kvc_snapkv_params *p, int32_t num_sms, int64_t *out);
+
 /* For every unit (layer, batch b, KV head h):
  *   1. window scores: each of the Wq trailing queries of the G query heads of h, at
  *      position i = L - Wq + r, takes softmax over the keys 0..i (prefix keys always,
