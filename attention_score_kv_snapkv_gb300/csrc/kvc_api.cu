@@ -121,10 +121,15 @@ kvc_status plan_snapkv(const kvc_snapkv_params *p, bool want_scores, int num_sms
   return KVC_OK;
 }
 
+// SM count of the current device for sizing queries, or 160 without a usable device (a
+// failed lookup's error is cleared so that the caller's own error checks do not see it).
 int sms_for_sizing() {
   int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 160;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 160;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 160;
+  }
   return sms > 0 ? sms : 160;
 }
 
