@@ -109,3 +109,27 @@ def test_rejected_sizes_raise_with_the_call_codes():
     with pytest.raises(kvc.KVCError) as e:       # budget below the kept window
         kvc.snapkv_vote_plan(1, 1, 4, 4, 64, 100, 8, 16, 7, 12, num_sms=152)
     assert e.value.code == 4
+
+
+def test_h2o_step_plans_on_the_host():
+    """h2o_step_ctas_per_unit is host arithmetic too (160 SMs assumed without a device):
+    one CTA per unit for the OPT-6.7B-shaped step, the split step when a unit's logits do
+    not fit one CTA's shared memory, 0 for sizes the step rejects."""
+    assert kvc.h2o_step_ctas_per_unit(32, 64, 32, 32, 128, 204, 204) == 1
+    assert kvc.h2o_step_ctas_per_unit(8, 1, 32, 32, 128, 13107, 13107) > 1
+    assert kvc.h2o_step_ctas_per_unit(1, 1, 36, 4, 128, 8, 8) == 0      # 9 query heads per KV head
+    assert kvc.h2o_step_ctas_per_unit(1, 1, 4, 4, 128, 8, 0) == 0       # no recent window
+    assert kvc.h2o_step_ctas_per_unit(1, 1, 4, 4, 96, 8, 8) == 0        # head dim 96
+
+
+def test_readme_example_calls_existing_entry_points():
+    import os
+    import re
+    from conftest import ROOT
+    text = open(os.path.join(ROOT, "README.md")).read()
+    blocks = re.findall(r"```python\n(.*?)```", text, flags=re.S)
+    assert blocks
+    names = set(re.findall(r"kvc\.([a-z_0-9]+)\(", "".join(blocks)))
+    assert names
+    for n in sorted(names):
+        assert callable(getattr(kvc, n, None)), n
