@@ -59,11 +59,12 @@ constexpr float SLACK = 8.f;     // a row's reference moves only past this (log2
 constexpr float NOREF = 3.0e38f; // -ref of a row with no reference yet (finite, so that
                                  // s.c - ref is +huge for a finite logit and -inf for -inf)
 // Partial statistics a merging thread loads per batch.  Every CTA of a group reads all
-// g partials of a job at the same moment (152 CTAs x g x rows at g = 152), so the batch
-// trades the exchange's latency against a burst of L2 requests that also delays the key
-// stream.  Measured on the long-context prompt (8 layers, g = 152, 32 rows, 4 threads
-// per row): batches of 10 take 1.82 ms, against 1.93 ms with batches of 20, 1.85 / 1.84
-// ms with 8 / 13, 2.07 ms with 5 and about 2.3 ms with all 38 in one batch.
+// g partials of a job at the same moment (g x g x rows loads: 147 x 147 x 32 on the
+// long-context prompt), so the batch trades the exchange's latency against a burst of L2
+// requests that also delays the key stream.  Measured on that prompt (8 layers, g = 147,
+// 32 rows, 4 threads per row): batches of 10 take 1.82 ms, against 1.93 ms with batches
+// of 20, 1.85 / 1.84 ms with 8 / 13, 2.07 ms with 5 and about 2.3 ms with all 37 in one
+// batch.
 constexpr int XB = 10;
 
 // control region byte offsets
