@@ -716,7 +716,7 @@ bool g_attr_done[8][64];
 // that qualify, a round (every group on one job) costs about the busiest CTA's key
 // tiles, plus its Q tile (qr/128 of a key tile) and, when g > 1, the exchange.  Of equal
 // costs the smallest g is taken: its CTAs' shares are the most even.  Measured on the
-// long-context prompt (1024 key tiles per job, 8 layers): g = 147 (7 tiles on all but 4
+// long-context prompt (1024 key tiles per job, 8 layers): g = 147 (7 tiles on all but 5
 // CTAs) 1.82 ms, against 1.99 ms for g = 152 (6 or 7 tiles), 1.96 ms for g = 128 (8
 // each, tensor memory full with two jobs) and 2.16 ms for g = 140.
 constexpr int MIN_TPC = 4;
